@@ -1,0 +1,226 @@
+"""Plain CPU oracle of the MaskLLM 2:4 mask layer (ctypes wrapper over the C code).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``.  The product path (the CUDA library
+and its binding) never imports this package, and this package imports nothing
+from the product.
+
+All array arguments are numpy arrays on the host.  bf16 tensors travel as
+``uint16`` bit patterns.  Float outputs of the oracle are float64 (it computes
+in double after the fp32 logit arithmetic that defines z; see the C header).
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+
+from . import _build
+
+NCAND = 6
+TABLE_BITS = 14
+TABLE_SIZE = 1 << TABLE_BITS
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = C.CDLL(path)
+        u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
+        u32p = np.ctypeslib.ndpointer(np.uint32, flags="C_CONTIGUOUS")
+        f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+        f64p = np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")
+        u8p = np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")
+        i64, u64, u32, f32 = C.c_int64, C.c_uint64, C.c_uint32, C.c_float
+        vp = C.c_void_p
+        L.orc_candidate_pair.argtypes = [C.c_int, C.c_int]
+        L.orc_candidate_pair.restype = C.c_int
+        L.orc_candidate_keeps.argtypes = [C.c_int, C.c_int]
+        L.orc_candidate_keeps.restype = C.c_int
+        L.orc_bf16_to_double.argtypes = [C.c_uint16]
+        L.orc_bf16_to_double.restype = C.c_double
+        L.orc_double_to_bf16.argtypes = [C.c_double]
+        L.orc_double_to_bf16.restype = C.c_uint16
+        L.orc_philox4x32_10.argtypes = [u32p, u32p, u32p]
+        L.orc_philox4x32_10.restype = None
+        L.orc_noise_words.argtypes = [u64, u32, u32, i64, i64, u32p]
+        L.orc_noise_words.restype = None
+        L.orc_gumbel_table.argtypes = [f32p]
+        L.orc_gumbel_table.restype = None
+        L.orc_gumbel_noise.argtypes = [u64, u32, u32, i64, i64, f32p]
+        L.orc_gumbel_noise.restype = None
+        L.orc_gumbel_cell.argtypes = [u32p, C.c_int]
+        L.orc_gumbel_cell.restype = C.c_int
+        L.orc_group_probs.argtypes = [f32p, f32p, f32, f32, C.c_int, f64p, vp]
+        L.orc_group_probs.restype = None
+        L.orc_soft_mask.argtypes = [f64p, f64p]
+        L.orc_soft_mask.restype = None
+        L.orc_group_backward.argtypes = [f64p, f64p, f64p, C.c_double, f64p]
+        L.orc_group_backward.restype = None
+        L.orc_prior_init.argtypes = [u16p, i64, i64, f32, f32p]
+        L.orc_prior_init.restype = None
+        L.orc_forward.argtypes = [u16p, f32p, i64, i64, i64, f32, f32, u64, u32, u32,
+                                  u16p, vp, vp, vp]
+        L.orc_forward.restype = None
+        L.orc_backward.argtypes = [u16p, f32p, u16p, i64, i64, i64, f32, f32, u64, u32,
+                                   u32, f32, C.c_int, f64p]
+        L.orc_backward.restype = None
+        L.orc_loss_exact.argtypes = [u16p, f32p, u16p, i64, i64, i64, f32, f32, u64, u32,
+                                     u32, f32]
+        L.orc_loss_exact.restype = C.c_double
+        L.orc_hard_index.argtypes = [f32p]
+        L.orc_hard_index.restype = C.c_int
+        L.orc_hard_compress.argtypes = [u16p, f32p, i64, i64, u16p, u32p, vp]
+        L.orc_hard_compress.restype = None
+        L.orc_decompress.argtypes = [u16p, u32p, i64, i64, u16p]
+        L.orc_decompress.restype = None
+        L.orc_compressed_bytes.argtypes = [i64, i64, i64]
+        L.orc_compressed_bytes.restype = i64
+        _ = u8p
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def candidate_pairs():
+    """The six kept index pairs in the oracle's candidate order."""
+    return [(lib().orc_candidate_pair(c, 0), lib().orc_candidate_pair(c, 1))
+            for c in range(NCAND)]
+
+
+def bf16_to_f64(bits):
+    bits = np.asarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def double_to_bf16(x: float) -> int:
+    return int(lib().orc_double_to_bf16(float(x)))
+
+
+def philox4x32_10(key, ctr):
+    out = np.zeros(4, np.uint32)
+    lib().orc_philox4x32_10(_c(key, np.uint32), _c(ctr, np.uint32), out)
+    return out
+
+
+def noise_words(seed: int, step: int, tensor_id: int, group_begin: int, n: int):
+    out = np.zeros((n, 4), np.uint32)
+    lib().orc_noise_words(seed, step, tensor_id, group_begin, n, out)
+    return out
+
+
+def gumbel_table():
+    t = np.zeros(TABLE_SIZE, np.float32)
+    lib().orc_gumbel_table(t)
+    return t
+
+
+def gumbel_noise(seed: int, step: int, tensor_id: int, group_begin: int, n: int):
+    out = np.zeros((n, NCAND), np.float32)
+    lib().orc_gumbel_noise(seed, step, tensor_id, group_begin, n, out)
+    return out
+
+
+def gumbel_cell(words, c: int) -> int:
+    return int(lib().orc_gumbel_cell(_c(words, np.uint32), c))
+
+
+def group_probs(logits, gumbel, kappa: float, tau: float, exact: bool = False):
+    p = np.zeros(NCAND, np.float64)
+    z = np.zeros(NCAND, np.float64)
+    lib().orc_group_probs(_c(logits, np.float32), _c(gumbel, np.float32), kappa, tau,
+                          int(exact), p, _ptr(z))
+    return p, z
+
+
+def soft_mask(p):
+    m = np.zeros(4, np.float64)
+    lib().orc_soft_mask(_c(p, np.float64), m)
+    return m
+
+
+def group_backward(p, w, t, dz_dlogit: float):
+    out = np.zeros(NCAND, np.float64)
+    lib().orc_group_backward(_c(p, np.float64), _c(w, np.float64), _c(t, np.float64),
+                             float(dz_dlogit), out)
+    return out
+
+
+def prior_init(W, scale: float):
+    W = _c(W, np.uint16)
+    rows, cols = W.shape
+    out = np.zeros((rows, cols // 4, NCAND), np.float32)
+    lib().orc_prior_init(W, rows, cols, scale, out)
+    return out
+
+
+def forward(W, L, tau, kappa, seed, step=0, tensor_id=0, row_begin=0,
+            want_probs=False, want_masks=False):
+    """Returns (W_out bf16 bits [rows, cols], row_sq f64 [rows], probs|None, masks|None)."""
+    W = _c(W, np.uint16)
+    rows, cols = W.shape
+    L = _c(L, np.float32).reshape(rows, cols // 4, NCAND)
+    W_out = np.zeros((rows, cols), np.uint16)
+    row_sq = np.zeros(rows, np.float64)
+    probs = np.zeros((rows, cols // 4, NCAND), np.float64) if want_probs else None
+    masks = np.zeros((rows, cols), np.float64) if want_masks else None
+    lib().orc_forward(W, L, rows, cols, row_begin, tau, kappa, seed, step, tensor_id,
+                      W_out, _ptr(row_sq), _ptr(probs), _ptr(masks))
+    return W_out, row_sq, probs, masks
+
+
+def backward(W, L, G, tau, kappa, seed, step=0, tensor_id=0, reg_coeff=0.0, row_begin=0,
+             exact=False):
+    W = _c(W, np.uint16)
+    rows, cols = W.shape
+    L = _c(L, np.float32).reshape(rows, cols // 4, NCAND)
+    G = _c(G, np.uint16)
+    out = np.zeros((rows, cols // 4, NCAND), np.float64)
+    lib().orc_backward(W, L, G, rows, cols, row_begin, tau, kappa, seed, step, tensor_id,
+                       reg_coeff, int(exact), out)
+    return out
+
+
+def loss_exact(W, L, G, tau, kappa, seed, step=0, tensor_id=0, reg_coeff=0.0, row_begin=0):
+    W = _c(W, np.uint16)
+    rows, cols = W.shape
+    L = _c(L, np.float32).reshape(rows, cols // 4, NCAND)
+    G = _c(G, np.uint16)
+    return lib().orc_loss_exact(W, L, G, rows, cols, row_begin, tau, kappa, seed, step,
+                                tensor_id, reg_coeff)
+
+
+def hard_index(logits6) -> int:
+    return int(lib().orc_hard_index(_c(logits6, np.float32)))
+
+
+def hard_compress(W, L):
+    """Returns (values bf16 bits [rows, cols/2], meta u32 [rows, cols/32], idx u8 [rows, cols/4])."""
+    W = _c(W, np.uint16)
+    rows, cols = W.shape
+    L = _c(L, np.float32).reshape(rows, cols // 4, NCAND)
+    vals = np.zeros((rows, cols // 2), np.uint16)
+    meta = np.zeros((rows, cols // 32), np.uint32)
+    idx = np.zeros((rows, cols // 4), np.uint8)
+    lib().orc_hard_compress(W, L, rows, cols, vals, meta, _ptr(idx))
+    return vals, meta, idx
+
+
+def decompress(vals, meta, rows: int, cols: int):
+    out = np.zeros((rows, cols), np.uint16)
+    lib().orc_decompress(_c(vals, np.uint16), _c(meta, np.uint32), rows, cols, out)
+    return out
+
+
+def compressed_bytes(rows: int, cols: int, elem_bytes: int) -> int:
+    return int(lib().orc_compressed_bytes(rows, cols, elem_bytes))
