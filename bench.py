@@ -1,0 +1,527 @@
+#!/usr/bin/env python
+"""Throughput of the MaskLLM 2:4 mask layer on GB300.
+
+One step = one pass of the whole hot path over the seven linears of a
+LLaMA-2-7B block (202,375,168 weights, inputs resident in HBM):
+magnitude prior -> forward (W', row sum of squares) -> backward (dlogits)
+-> hard mask + 2:4 compression, each kernel over all seven matrices.
+
+Prints one JSON line (rank 0).  `value` is whole-job weights per second
+(all ranks); `e2e` is the same step through the C ABI with the inputs copied
+from pinned host memory and every output copied back inside the timed region;
+`roofline` is the dominant kernel's algorithmic bytes per launch over its
+CUDA-event launch time against the measured HBM copy bandwidth;
+`cpu_baseline` times the CPU oracle on a bounded sample of the same workload.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl gpu|reference]
+For N > 1 launch one process per GPU with torch.distributed.run; each rank
+processes its own block (a different layer's tensors: weak scaling, no
+collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+# Algorithmic bytes per weight of each kernel (what the method must move).
+BYTES_PER_WEIGHT = {"prior": 8.0, "forward": 10.0, "backward": 16.0, "hard_compress": 9.125}
+KERNELS = ("prior", "forward", "backward", "hard_compress")
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "weights/s (prior + forward + backward + hard-compress step)"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gpu", "reference"), default="gpu")
+    ap.add_argument("--workload", default="llama2_7b_block")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------
+
+class Ranks:
+    def __init__(self, backend_gpu: bool):
+        import torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            backend = "nccl" if backend_gpu else "gloo"
+            if backend_gpu:
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        return reduce_max(self.pg, x)
+
+    def sum(self, x: float) -> float:
+        return reduce_sum(self.pg, x)
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def _reduce(pg, x: float, op_name: str) -> float:
+    if pg is None:
+        return x
+    import torch
+    dev = "cuda" if pg.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=getattr(pg.ReduceOp, op_name))
+    return float(t.item())
+
+
+def reduce_max(pg, x: float) -> float:
+    """Max of a per-rank value (the job's time is its slowest rank's)."""
+    return _reduce(pg, x, "MAX")
+
+
+def reduce_sum(pg, x: float) -> float:
+    return _reduce(pg, x, "SUM")
+
+
+def job_value(weights_per_rank: int, world: int, max_seconds: float, steps: int) -> float:
+    """Whole-job throughput: the weights all ranks processed over the slowest rank's time."""
+    return weights_per_rank * world * steps / max_seconds
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_table():
+    """Per-launch DRAM bytes from the committed ncu summary, keyed by kernel
+    and matrix shape, valid only for the kernel source it was taken on."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    out = {}
+    try:
+        with open(path) as f:
+            for line in f:
+                p = line.split()
+                if len(p) == 5 and p[0] == "traffic":
+                    out[(p[1], p[2])] = (float(p[3]), p[4])
+    except OSError:
+        pass
+    return out
+
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "semi_structured_sparsity_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:12]
+
+
+# ---------------------------------------------------------------------------
+# the step
+# ---------------------------------------------------------------------------
+
+class Block:
+    """Resident inputs and outputs of one block of matrices on one GPU."""
+
+    def __init__(self, wl, layer, device):
+        import torch
+
+        from semi_structured_sparsity_gb300 import binding as mk
+        from semi_structured_sparsity_gb300 import workloads as W
+        self.mk, self.wl, self.dev = mk, wl, device
+        self.mats = []
+        for m in range(len(wl.matrices)):
+            x = W.matrix_inputs(wl, layer, m, device=device)
+            if x.L is None:   # logits = magnitude prior + noise
+                x.L = mk.maskllm_prior_init(x.W, wl.prior_scale) + x.L_noise
+                x.L_noise = None
+            r, c = x.rows, x.cols
+            self.mats.append({
+                "x": x,
+                "L_prior": torch.empty((r, c // 4, 6), dtype=torch.float32, device=device),
+                "W_out": torch.empty((r, c), dtype=torch.bfloat16, device=device),
+                "row_sq": torch.empty((r,), dtype=torch.float32, device=device),
+                "dL": torch.empty((r, c // 4, 6), dtype=torch.float32, device=device),
+                "vals": torch.empty((r, c // 2), dtype=torch.bfloat16, device=device),
+                "meta": torch.empty((r, c // 32), dtype=torch.int32, device=device),
+            })
+        torch.cuda.synchronize(device)
+        self.weights = sum(m["x"].rows * m["x"].cols for m in self.mats)
+        self.launches = 0
+
+    def run(self, step: int, events=None):
+        """Launch the four kernels over every matrix; events[k] = (start, end)
+        CUDA events bracketing kernel k's launches (optional)."""
+        mk, wl = self.mk, self.wl
+        for k in KERNELS:
+            if events is not None:
+                events[k][0].record()
+            for m in self.mats:
+                x = m["x"]
+                rng = (0, step, x.tensor_id)
+                if k == "prior":
+                    mk.maskllm_prior_init(x.W, wl.prior_scale or 1.0, logits_out=m["L_prior"])
+                elif k == "forward":
+                    mk.maskllm_forward(x.W, x.L, wl.tau, wl.kappa, rng, W_out=m["W_out"],
+                                       row_sq_out=m["row_sq"])
+                elif k == "backward":
+                    mk.maskllm_backward(x.W, x.L, x.G, wl.tau, wl.kappa, rng,
+                                        dlogits_out=m["dL"])
+                else:
+                    mk.maskllm_hard_compress(x.W, x.L, values_out=m["vals"], meta_out=m["meta"])
+                self.launches += 1
+            if events is not None:
+                events[k][1].record()
+
+
+def run_gpu(args):
+    import torch
+
+    from semi_structured_sparsity_gb300 import _build
+    from semi_structured_sparsity_gb300 import workloads as W
+    _build.build()
+    ranks = Ranks(backend_gpu=True)
+    dev = torch.device("cuda", ranks.local)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]
+    blk = Block(wl, layer=ranks.rank % max(wl.layers, 1), device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for s in range(args.warmup):
+        blk.run(s)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    ev = {k: [] for k in KERNELS}
+    ranks.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    launches0 = blk.launches
+    t0.record(stream)
+    for s in range(args.steps):
+        e = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for k in KERNELS}
+        blk.run(args.warmup + s, events=e)
+        for k in KERNELS:
+            ev[k].append(e[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ranks.barrier()
+    clk = clocks.stop()
+    launches = blk.launches - launches0
+    sec = t0.elapsed_time(t1) / 1e3
+    sec_max = ranks.max(sec)
+    per_kernel_s = {k: sum(a.elapsed_time(b) for a, b in ev[k]) / 1e3 / args.steps
+                    for k in KERNELS}
+    value = job_value(blk.weights, ranks.world, sec_max, args.steps)
+
+    peak, peak_kind = hbm_peak()
+    kernels = {}
+    for k in KERNELS:
+        gbs = BYTES_PER_WEIGHT[k] * blk.weights / per_kernel_s[k] / 1e9
+        kernels[k] = {"us_per_step": round(per_kernel_s[k] * 1e6, 2),
+                      "weights_per_s": blk.weights / per_kernel_s[k],
+                      "GB_per_s": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
+    dominant = max(KERNELS, key=lambda k: per_kernel_s[k])
+    # per launch = one matrix; report the dominant kernel over the block's
+    # launches: bytes of all its launches over the summed launch time
+    ach = BYTES_PER_WEIGHT[dominant] * blk.weights / per_kernel_s[dominant] / 1e9
+    tt = traffic_table()
+    digest = kernel_source_digest()
+    traffic = None
+    shape_key = "%s" % args.workload
+    if (dominant, shape_key) in tt and tt[(dominant, shape_key)][1] == digest:
+        traffic = tt[(dominant, shape_key)][0]
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, blk, ranks, dev)
+
+    cpu = None
+    if not args.no_cpu_baseline and ranks.rank == 0 and ranks.world == 1:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "weights/s",
+        "n_gpus": ranks.world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": sec_max / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 weights, fp32 logits",
+        "data": "synthetic (seeded; LLaMA-2-7B block shapes, W~N(0,0.02), logits = magnitude "
+                "prior(300) + N(0,0.1), G~N(0,1e-3))",
+        "config": {"workload": args.workload, "weights_per_gpu": blk.weights,
+                   "matrices": [list(m[1:]) for m in wl.matrices], "tau": wl.tau,
+                   "kappa": wl.kappa, "parallelism": "dp%d (independent blocks)" % ranks.world,
+                   "l2": "inputs larger than L2 (per-kernel sweep reads >= 1.6 GB)"},
+        "kernels": kernels,
+        "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(ach, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(ach / peak, 4), "traffic": traffic,
+                     "bytes_per_weight": BYTES_PER_WEIGHT[dominant],
+                     "launches_per_step": len(blk.mats)},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if ranks.rank == 0:
+        print(json.dumps(line), flush=True)
+    ranks.close()
+
+
+def run_e2e(args, blk, ranks, dev):
+    """The same step through the C ABI with host buffers: every step copies
+    W, logits and G from pinned host memory, runs the four kernels, and copies
+    every output back to pinned host memory."""
+    import torch
+    host_in, host_out = [], []
+    for m in blk.mats:
+        x = m["x"]
+        host_in.append([t.cpu().pin_memory() for t in (x.W, x.L, x.G)])
+        host_out.append([torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                         for t in (m["L_prior"], m["W_out"], m["row_sq"], m["dL"], m["vals"],
+                                   m["meta"])])
+    h2d = sum(t.numel() * t.element_size() for h in host_in for t in h)
+    d2h = sum(t.numel() * t.element_size() for h in host_out for t in h)
+    stream = torch.cuda.current_stream(dev)
+
+    def one(step):
+        for m, hin in zip(blk.mats, host_in):
+            x = m["x"]
+            for dst, src in zip((x.W, x.L, x.G), hin):
+                dst.copy_(src, non_blocking=True)
+        blk.run(step)
+        for m, hout in zip(blk.mats, host_out):
+            for dst, src in zip(hout, (m["L_prior"], m["W_out"], m["row_sq"], m["dL"],
+                                       m["vals"], m["meta"])):
+                dst.copy_(src, non_blocking=True)
+
+    one(0)
+    torch.cuda.synchronize(dev)
+    ranks.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(args.e2e_steps):
+        one(s + 1)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ranks.barrier()
+    sec = ranks.max(t0.elapsed_time(t1) / 1e3)
+    return {"value": job_value(blk.weights, ranks.world, sec, args.e2e_steps),
+            "unit": "weights/s", "steps": args.e2e_steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step(wl, rows_per_matrix: int, layer: int = 0):
+    """CPU inputs of `rows_per_matrix` rows of every matrix of the workload,
+    drawn with the workload's distributions and per-tensor seeds."""
+    from semi_structured_sparsity_gb300 import workloads as W
+    import oracle as orc
+    out = []
+    for m, (name, rows, cols) in enumerate(wl.matrices):
+        n = min(rows_per_matrix, rows)
+        seed = lambda role: W.tensor_seed(wl.index, layer, m, role)
+        Wb = W.bf16_bits(W.normal_bf16(n, cols, wl.w_sigma, seed(W.ROLE_W)))
+        Gb = W.bf16_bits(W.normal_bf16(n, cols, wl.g_sigma, seed(W.ROLE_G)))
+        if wl.logits == "prior":
+            noise = W.normal_f32((n, cols // 4, 6), wl.l_sigma, seed(W.ROLE_L)).numpy()
+            L = orc.prior_init(Wb, wl.prior_scale) + noise
+        elif wl.logits == "onehot":
+            L = W.onehot_logits(n, cols, seed(W.ROLE_L)).numpy()
+        else:
+            L = W.normal_f32((n, cols // 4, 6), wl.l_sigma, seed(W.ROLE_L)).numpy()
+        out.append((Wb, L.astype("float32"), Gb, W.noise_tensor_id(layer, m)))
+    return out
+
+
+def oracle_step(wl, sample, step: int):
+    import oracle as orc
+    for Wb, L, Gb, tid in sample:
+        orc.prior_init(Wb, wl.prior_scale or 1.0)
+        orc.forward(Wb, L, wl.tau, wl.kappa, 0, step, tid)
+        orc.backward(Wb, L, Gb, wl.tau, wl.kappa, 0, step, tid)
+        orc.hard_compress(Wb, L)
+
+
+def cpu_baseline(wl, target_seconds: float):
+    """The oracle, as it stands, single-threaded, on a bounded sample: the
+    first k rows of every matrix of the block, k grown until the timed pass
+    takes about `target_seconds`."""
+    k = 1
+    while True:
+        sample = oracle_sample_step(wl, k)
+        t = time.perf_counter()
+        oracle_step(wl, sample, 0)
+        dt = time.perf_counter() - t
+        if dt >= target_seconds or k >= 4096:
+            break
+        k = min(4096, max(k + 1, int(k * min(8.0, 1.2 * target_seconds / max(dt, 1e-3)))))
+    weights = sum(s[0].size for s in sample)
+    return {"value": weights / dt, "unit": "weights/s", "cores": 1, "kind": "oracle",
+            "sample": "first %d rows of each of the %d matrices (%d weights), one full "
+                      "prior+forward+backward+compress pass, %.1f s" % (
+                          k, len(sample), weights, dt)}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step runs prior, forward,
+    backward and compress on a bounded sample (the first k rows of every
+    matrix), sized so the whole --warmup + --steps run stays within minutes."""
+    ranks_world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from semi_structured_sparsity_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    total_steps = args.warmup + args.steps
+    budget = 120.0 / max(total_steps, 1)       # seconds of CPU per step
+    k = 1
+    while True:
+        sample = oracle_sample_step(wl, k)
+        t = time.perf_counter()
+        oracle_step(wl, sample, 0)
+        dt = time.perf_counter() - t
+        if dt >= 0.5 * budget or k >= 4096:
+            break
+        k *= 2
+    for s in range(args.warmup):
+        oracle_step(wl, sample, s)
+    t = time.perf_counter()
+    for s in range(args.steps):
+        oracle_step(wl, sample, args.warmup + s)
+    sec = time.perf_counter() - t
+    weights = sum(x[0].size for x in sample)
+    value = weights * args.steps / sec
+    desc = "first %d rows of each of the %d matrices (%d weights) per step" % (
+        k, len(sample), weights)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "weights/s",
+        "n_gpus": ranks_world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 weights, fp32 logits (oracle computes in fp64)",
+        "data": "synthetic (seeded, same recipe as the GPU arm)",
+        "config": {"workload": args.workload, "weights_per_step": weights},
+        "cpu_baseline": {"value": value, "unit": "weights/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "weights/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * maskllm.h -- C ABI of libmaskllm: MaskLLM's differentiable 2:4 mask layer
+ * on NVIDIA GB300 (sm_103a).
+ *
+ * The method.  "MaskLLM: Learnable Semi-Structured Sparsity for Large Language
+ * Models" (project page), Fig. 3: every group of M = 4 consecutive weights of
+ * a frozen matrix carries a learnable categorical distribution over the
+ * candidate 2:4 masks; a mask is drawn with the Gumbel softmax and the
+ * candidates are averaged with its weights, all differentiably.  Fig. 5: the
+ * logits are scaled by kappa, which sets the randomness of the draw.  Table 2:
+ * prior masks initialise the logits.  Table 3: a weight regulariser helps.
+ * "Accelerating Sparse Deep Neural Networks" (Mishra et al.), Sec. 3.1: a 2:4
+ * matrix is stored as the two kept values of each group of four plus 2 bits of
+ * position metadata per kept value; Sec. 4.1: magnitude pruning keeps the two
+ * largest of four.
+ *
+ * Notation used below.
+ *   W        frozen weights, bf16, [rows, cols] row-major (bf16 values travel
+ *            as their uint16_t bit patterns).  cols % 32 == 0.
+ *   group    k-th group of row r = W[r, 4k .. 4k+3]; its index within the
+ *            matrix is  gidx = r * (cols/4) + k.
+ *   candidates  the six kept index pairs in lexicographic order
+ *            c0 (0,1)  c1 (0,2)  c2 (0,3)  c3 (1,2)  c4 (1,3)  c5 (2,3).
+ *   logits   L, fp32, [rows, cols/4, 6] row-major (24 bytes per group).
+ *   noise    g_c, Gumbel(0,1) quantised to 2^14 cells: the four words
+ *            Philox4x32-10(key = (seed lo, seed hi),
+ *                           counter = (gidx lo, gidx hi, step, tensor_id));
+ *            candidate c takes 16-bit half (c & 1) of word (c >> 1) (low half
+ *            for even c), cell = its top 14 bits, g_c = fl32(-ln(-ln((cell +
+ *            0.5) / 2^14))).  Word 3 is unused.  The noise is a pure function
+ *            of (rng, gidx), so the forward and the backward of one step draw
+ *            the same noise; it is never stored.
+ *   z_c      = fl32(fl32(fl32(kappa * L_c) + g_c) * rho), rho = fl32(1/tau).
+ *   p        = softmax(z);  M_j = sum over candidates c keeping j of p_c.
+ *
+ * Conventions shared by every call.
+ *   - Every pointer is a DEVICE pointer owned by the caller, 16-byte aligned.
+ *     The library never allocates, frees or keeps device memory of the
+ *     caller.  Inputs are read only; outputs are overwritten, never
+ *     accumulated into.  An output may not overlap any input or another
+ *     output.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and returns after the launch; nothing
+ *     synchronises.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns its error and launches nothing.  After the launch
+ *     cudaGetLastError() is checked; a launch failure returns
+ *     MASKLLM_ERR_CUDA (maskllm_last_cuda_error() gives the CUDA message).
+ *   - Shapes: rows >= 1, cols >= 32, cols % 32 == 0, rows * cols < 2^46.
+ *     (The multiple of 32 follows the page's rule that pruned GEMM
+ *     dimensions are multiples of 16/32, and makes the 32-bit metadata words
+ *     of a row whole.)
+ */
+#ifndef MASKLLM_H_
+#define MASKLLM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (both are `struct CUstream_st *`). */
+typedef struct CUstream_st* maskllm_stream_t;
+
+typedef enum {
+  MASKLLM_OK = 0,
+  MASKLLM_ERR_INVALID_ARG = 1, /* null pointer, non-finite or out-of-range scalar */
+  MASKLLM_ERR_SHAPE = 2,       /* rows/cols outside the rules above */
+  MASKLLM_ERR_ALIGNMENT = 3,   /* a pointer not 16-byte aligned */
+  MASKLLM_ERR_ALIAS = 4,       /* an output overlaps an input or another output */
+  MASKLLM_ERR_CUDA = 5,        /* the CUDA runtime reported an error */
+  MASKLLM_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up */
+} maskllm_status;
+
+/* Stateless RNG coordinates of one draw.  seed selects the key; step and
+ * tensor_id the counter's high words (one noise stream per training step and
+ * per weight matrix). */
+typedef struct {
+  uint64_t seed;
+  uint32_t step;
+  uint32_t tensor_id;
+} maskllm_rng;
+
+/* Magnitude prior (MaskLLM Table 2: prior masks initialise the logits;
+ * Mishra et al. Sec. 4.1: magnitude pruning).
+ *   logits_out[r, k, c] = fl32(scale * fl32(|w_i| + |w_j|)), (i, j) = pair c
+ * so the argmax candidate keeps the two largest magnitudes of the group.
+ *   W           in   bf16 [rows, cols]
+ *   scale       in   finite
+ *   logits_out  out  fp32 [rows, cols/4, 6]
+ * Moves 8 bytes per weight. */
+maskllm_status maskllm_prior_init(const uint16_t* W, int64_t rows, int64_t cols, float scale,
+                                  float* logits_out, maskllm_stream_t stream);
+
+/* Forward of the differentiable mask (MaskLLM Fig. 3, Fig. 5, Table 3):
+ *   x_j = fl32(w_j * M_j),  W_out_j = bf16 round-to-nearest-even of x_j,
+ *   row_sq_out[r] = sum over the row of x_j^2 (the weight regulariser's
+ *                   per-row value; deterministic for a given shape).
+ *   W           in   bf16 [rows, cols]
+ *   logits      in   fp32 [rows, cols/4, 6]
+ *   tau         in   > 0, finite (Gumbel-softmax temperature)
+ *   kappa       in   finite (logit scale)
+ *   rng         in   noise coordinates (see the notation above)
+ *   W_out       out  bf16 [rows, cols]
+ *   row_sq_out  out  fp32 [rows], or NULL to skip
+ *   probs_out   out  fp32 [rows, cols/4, 6] = p, or NULL (debug output;
+ *                    adds 24 bytes per group of traffic)
+ * Moves 10 bytes per weight (W 2, logits 6, W_out 2). */
+maskllm_status maskllm_forward(const uint16_t* W, const float* logits, int64_t rows,
+                               int64_t cols, float tau, float kappa, maskllm_rng rng,
+                               uint16_t* W_out, float* row_sq_out, float* probs_out,
+                               maskllm_stream_t stream);
+
+/* Backward of the mask (MaskLLM Fig. 3: every step is differentiable).  The
+ * loss seen by the layer is  l = <G, W_out> + reg_coeff * sum x^2  with the
+ * bf16 rounding of W_out passed straight through and the noise held fixed:
+ *   t_j = G_j + 2 reg_coeff x_j,  h_j = t_j w_j,  dp_c = h_i + h_j,
+ *   r = sum_c p_c dp_c,  dlogits_c = (kappa * rho) p_c (dp_c - r).
+ * Must be called with the same rng, tau and kappa as the forward it
+ * differentiates (it redraws the same noise).
+ *   W           in   bf16 [rows, cols]
+ *   logits      in   fp32 [rows, cols/4, 6]
+ *   grad_W_out  in   bf16 [rows, cols] = dl/dW_out
+ *   reg_coeff   in   finite (0 disables the regulariser term exactly)
+ *   dlogits_out out  fp32 [rows, cols/4, 6] (overwritten)
+ * Moves 16 bytes per weight (W 2, logits 6, grad 2, dlogits 6). */
+maskllm_status maskllm_backward(const uint16_t* W, const float* logits,
+                                const uint16_t* grad_W_out, int64_t rows, int64_t cols,
+                                float tau, float kappa, maskllm_rng rng, float reg_coeff,
+                                float* dlogits_out, maskllm_stream_t stream);
+
+/* Hard mask and 2:4 compression (MaskLLM: the learned distribution's most
+ * likely candidate is the deployed mask; Mishra et al. Sec. 3.1 storage).
+ *   c* = argmax_c logits[r, k, c] over the raw logits (no noise, no kappa or
+ *        tau), lowest index on ties; a NaN logit never wins; six NaNs give 0.
+ *   values_out[r, 2k], values_out[r, 2k+1] = w_i, w_j for (i, j) = pair c*
+ *   meta_out[r, k/8] bits 4(k%8) .. 4(k%8)+3 = i | j << 2
+ *   W           in   bf16 [rows, cols]
+ *   logits      in   fp32 [rows, cols/4, 6]
+ *   values_out  out  bf16 [rows, cols/2]
+ *   meta_out    out  uint32 [rows, cols/32]
+ *   idx_out     out  uint8 [rows, cols/4] = c*, or NULL to skip
+ * Moves 9.125 bytes per weight (W 2, logits 6, values 1, meta 0.125). */
+maskllm_status maskllm_hard_compress(const uint16_t* W, const float* logits, int64_t rows,
+                                     int64_t cols, uint16_t* values_out, uint32_t* meta_out,
+                                     uint8_t* idx_out, maskllm_stream_t stream);
+
+/* Inverse of the storage above: W_out = the kept values in place, +0 (0x0000)
+ * at the two dropped positions of every group.
+ *   values  in   bf16 [rows, cols/2]
+ *   meta    in   uint32 [rows, cols/32]; every 4-bit code must have i < j
+ *   W_out   out  bf16 [rows, cols] */
+maskllm_status maskllm_decompress(const uint16_t* values, const uint32_t* meta, int64_t rows,
+                                  int64_t cols, uint16_t* W_out, maskllm_stream_t stream);
+
+/* The four Philox4x32-10 noise words of groups [group_begin, group_begin + n)
+ * (see the notation above), for checking the noise stream.
+ *   group_begin >= 0, n >= 1
+ *   out4  out  uint32 [n, 4] */
+maskllm_status maskllm_noise_words(maskllm_rng rng, int64_t group_begin, int64_t n,
+                                   uint32_t* out4, maskllm_stream_t stream);
+
+/* Waits for `stream`, then reads and clears the library's device error word
+ * on the current device.  Returns MASKLLM_ERR_TIMEOUT if a bounded wait inside
+ * a kernel gave up since the last call (its results are then invalid),
+ * MASKLLM_ERR_CUDA if the wait itself failed, MASKLLM_OK otherwise. */
+maskllm_status maskllm_device_status(maskllm_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* maskllm_status_string(maskllm_status status);
+
+/* The CUDA error message of the last MASKLLM_ERR_CUDA returned to this host
+ * thread, or "" (thread-local static storage). */
+const char* maskllm_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MASKLLM_H_ */

@@ -1,0 +1,194 @@
+"""Thin Python binding of libmaskllm (include/maskllm.h), via ctypes.
+
+Argument marshalling only: every function checks the torch tensors it is given
+(device, dtype, shape, contiguity), allocates outputs that were not passed in
+(PyTorch is the device allocator), and calls the C entry point of the same
+name on the current CUDA stream.  No step of the computation runs here.  If
+``libmaskllm.so`` has not been built, ``lib()`` raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmaskllm.so")
+
+MASKLLM_OK = 0
+STATUS = {0: "MASKLLM_OK", 1: "MASKLLM_ERR_INVALID_ARG", 2: "MASKLLM_ERR_SHAPE",
+          3: "MASKLLM_ERR_ALIGNMENT", 4: "MASKLLM_ERR_ALIAS", 5: "MASKLLM_ERR_CUDA",
+          6: "MASKLLM_ERR_TIMEOUT"}
+
+# The entry points of include/maskllm.h, in declaration order.
+EXPORTS = ("maskllm_prior_init", "maskllm_forward", "maskllm_backward",
+           "maskllm_hard_compress", "maskllm_decompress", "maskllm_noise_words",
+           "maskllm_device_status", "maskllm_status_string", "maskllm_last_cuda_error")
+
+
+class maskllm_rng(C.Structure):
+    _fields_ = [("seed", C.c_uint64), ("step", C.c_uint32), ("tensor_id", C.c_uint32)]
+
+
+class MaskLLMError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        msg = "%s returned %s" % (fn, STATUS.get(status, str(status)))
+        super().__init__(msg + (": " + detail if detail else ""))
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load libmaskllm.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libmaskllm.so is not built (%s); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+        L = C.CDLL(LIB_PATH)
+        vp, i64, f32, st = C.c_void_p, C.c_int64, C.c_float, C.c_int
+        L.maskllm_prior_init.argtypes = [vp, i64, i64, f32, vp, vp]
+        L.maskllm_forward.argtypes = [vp, vp, i64, i64, f32, f32, maskllm_rng, vp, vp, vp, vp]
+        L.maskllm_backward.argtypes = [vp, vp, vp, i64, i64, f32, f32, maskllm_rng, f32, vp, vp]
+        L.maskllm_hard_compress.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp]
+        L.maskllm_decompress.argtypes = [vp, vp, i64, i64, vp, vp]
+        L.maskllm_noise_words.argtypes = [maskllm_rng, i64, i64, vp, vp]
+        L.maskllm_device_status.argtypes = [vp]
+        for fn in EXPORTS[:7]:
+            getattr(L, fn).restype = st
+        L.maskllm_status_string.argtypes = [st]
+        L.maskllm_status_string.restype = C.c_char_p
+        L.maskllm_last_cuda_error.argtypes = []
+        L.maskllm_last_cuda_error.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != MASKLLM_OK:
+        detail = lib().maskllm_last_cuda_error().decode() if status == 5 else ""
+        raise MaskLLMError(fn, status, detail)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, name, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t
+
+
+def _out(t, name, dtype, shape, like):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    return _need(t, name, dtype, shape)
+
+
+def _rng(rng) -> maskllm_rng:
+    if isinstance(rng, maskllm_rng):
+        return rng
+    seed, step, tensor_id = rng
+    return maskllm_rng(seed, step, tensor_id)
+
+
+def maskllm_prior_init(W, scale, logits_out=None, stream=None):
+    rows, cols = W.shape
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    logits_out = _out(logits_out, "logits_out", torch.float32, (rows, cols // 4, 6), W)
+    _check("maskllm_prior_init", lib().maskllm_prior_init(
+        _ptr(W), rows, cols, scale, _ptr(logits_out), _stream(stream)))
+    return logits_out
+
+
+def maskllm_forward(W, logits, tau, kappa, rng, W_out=None, row_sq_out=None, probs_out=None,
+                    want_row_sq=True, stream=None):
+    rows, cols = W.shape
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    _need(logits, "logits", torch.float32, (rows, cols // 4, 6))
+    W_out = _out(W_out, "W_out", torch.bfloat16, (rows, cols), W)
+    if row_sq_out is None and want_row_sq:
+        row_sq_out = torch.empty((rows,), dtype=torch.float32, device=W.device)
+    elif row_sq_out is not None:
+        _need(row_sq_out, "row_sq_out", torch.float32, (rows,))
+    if probs_out is not None:
+        _need(probs_out, "probs_out", torch.float32, (rows, cols // 4, 6))
+    _check("maskllm_forward", lib().maskllm_forward(
+        _ptr(W), _ptr(logits), rows, cols, tau, kappa, _rng(rng), _ptr(W_out),
+        _ptr(row_sq_out), _ptr(probs_out), _stream(stream)))
+    return W_out, row_sq_out, probs_out
+
+
+def maskllm_backward(W, logits, grad_W_out, tau, kappa, rng, reg_coeff=0.0, dlogits_out=None,
+                     stream=None):
+    rows, cols = W.shape
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    _need(logits, "logits", torch.float32, (rows, cols // 4, 6))
+    _need(grad_W_out, "grad_W_out", torch.bfloat16, (rows, cols))
+    dlogits_out = _out(dlogits_out, "dlogits_out", torch.float32, (rows, cols // 4, 6), W)
+    _check("maskllm_backward", lib().maskllm_backward(
+        _ptr(W), _ptr(logits), _ptr(grad_W_out), rows, cols, tau, kappa, _rng(rng), reg_coeff,
+        _ptr(dlogits_out), _stream(stream)))
+    return dlogits_out
+
+
+def maskllm_hard_compress(W, logits, values_out=None, meta_out=None, idx_out=None,
+                          want_idx=False, stream=None):
+    rows, cols = W.shape
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    _need(logits, "logits", torch.float32, (rows, cols // 4, 6))
+    values_out = _out(values_out, "values_out", torch.bfloat16, (rows, cols // 2), W)
+    meta_out = _out(meta_out, "meta_out", torch.int32, (rows, cols // 32), W)
+    if idx_out is None and want_idx:
+        idx_out = torch.empty((rows, cols // 4), dtype=torch.uint8, device=W.device)
+    elif idx_out is not None:
+        _need(idx_out, "idx_out", torch.uint8, (rows, cols // 4))
+    _check("maskllm_hard_compress", lib().maskllm_hard_compress(
+        _ptr(W), _ptr(logits), rows, cols, _ptr(values_out), _ptr(meta_out), _ptr(idx_out),
+        _stream(stream)))
+    return values_out, meta_out, idx_out
+
+
+def maskllm_decompress(values, meta, rows, cols, W_out=None, stream=None):
+    _need(values, "values", torch.bfloat16, (rows, cols // 2))
+    _need(meta, "meta", torch.int32, (rows, cols // 32))
+    W_out = _out(W_out, "W_out", torch.bfloat16, (rows, cols), values)
+    _check("maskllm_decompress", lib().maskllm_decompress(
+        _ptr(values), _ptr(meta), rows, cols, _ptr(W_out), _stream(stream)))
+    return W_out
+
+
+def maskllm_noise_words(rng, group_begin, n, out4=None, device="cuda", stream=None):
+    if out4 is None:
+        out4 = torch.empty((n, 4), dtype=torch.int32, device=device)
+    else:
+        _need(out4, "out4", torch.int32, (n, 4))
+    _check("maskllm_noise_words", lib().maskllm_noise_words(
+        _rng(rng), group_begin, n, _ptr(out4), _stream(stream)))
+    return out4
+
+
+def maskllm_device_status(stream=None) -> int:
+    return int(lib().maskllm_device_status(_stream(stream)))
+
+
+def maskllm_status_string(status: int) -> str:
+    return lib().maskllm_status_string(status).decode()

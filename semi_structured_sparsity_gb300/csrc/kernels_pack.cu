@@ -1,0 +1,177 @@
+// kernels_pack.cu -- hard mask extraction, 2:4 compression and its inverse,
+// and the noise-word export.
+//
+// "MaskLLM: Learnable Semi-Structured Sparsity for Large Language Models":
+// the mask that is deployed is the learned distribution's most likely
+// candidate.  "Accelerating Sparse Deep Neural Networks", Sec. 3.1: a 2:4
+// matrix is stored as the two kept values of each group of four plus 2 bits
+// per kept value giving its position; the constant sparsity of every group
+// means fixed offsets and no data-dependent indirection.
+//
+// One work item is 8 groups = 32 weights = one 32-bit metadata word:
+// 64 bytes of W and 192 bytes of logits in, 32 bytes of values and 4 bytes
+// of metadata out (9.125 bytes per weight).
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace maskllm {
+namespace {
+
+// Candidate c's kept positions (i, j) and metadata code i | j << 2, packed one
+// nibble per candidate: c0 (0,1) c1 (0,2) c2 (0,3) c3 (1,2) c4 (1,3) c5 (2,3).
+constexpr uint32_t kPairI = 0x211000u;
+constexpr uint32_t kPairJ = 0x332321u;
+constexpr uint32_t kCode = 0xED9C84u;
+
+// argmax over the raw logits: the first maximum wins; a NaN never wins; six
+// NaNs select candidate 0.
+__device__ __forceinline__ int hard_index(const float L[kCand]) {
+  int best = 0;
+  float bv = L[0];
+  bool bnan = isnan(L[0]);
+#pragma unroll
+  for (int c = 1; c < kCand; ++c) {
+    if (!isnan(L[c]) && (bnan || L[c] > bv)) {
+      best = c;
+      bv = L[c];
+      bnan = false;
+    }
+  }
+  return best;
+}
+
+__device__ __forceinline__ uint32_t pick(uint32_t e0, uint32_t e1, uint32_t e2, uint32_t e3,
+                                         uint32_t k) {
+  return k == 0 ? e0 : (k == 1 ? e1 : (k == 2 ? e2 : e3));
+}
+
+__global__ void __launch_bounds__(256) hard_compress_kernel(
+    const uint4* __restrict__ W, const float4* __restrict__ L, uint4* __restrict__ vals,
+    uint32_t* __restrict__ meta, uint2* __restrict__ idx, int64_t items) {
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < items;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    uint32_t wd[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 w = __ldcs(W + 4 * q + v);
+      wd[4 * v + 0] = w.x;
+      wd[4 * v + 1] = w.y;
+      wd[4 * v + 2] = w.z;
+      wd[4 * v + 3] = w.w;
+    }
+    float lg[8 * kCand];
+#pragma unroll
+    for (int v = 0; v < 12; ++v) {
+      const float4 l = __ldcs(L + 12 * q + v);
+      lg[4 * v + 0] = l.x;
+      lg[4 * v + 1] = l.y;
+      lg[4 * v + 2] = l.z;
+      lg[4 * v + 3] = l.w;
+    }
+    uint32_t out[8];
+    uint32_t code_word = 0;
+    uint32_t idx_lo = 0, idx_hi = 0;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const int c = hard_index(lg + kCand * g);
+      const uint32_t i = (kPairI >> (4 * c)) & 0xFu;
+      const uint32_t j = (kPairJ >> (4 * c)) & 0xFu;
+      const uint32_t e0 = wd[2 * g] & 0xFFFFu, e1 = wd[2 * g] >> 16;
+      const uint32_t e2 = wd[2 * g + 1] & 0xFFFFu, e3 = wd[2 * g + 1] >> 16;
+      out[g] = pick(e0, e1, e2, e3, i) | (pick(e0, e1, e2, e3, j) << 16);
+      code_word |= ((kCode >> (4 * c)) & 0xFu) << (4 * g);
+      if (g < 4)
+        idx_lo |= static_cast<uint32_t>(c) << (8 * g);
+      else
+        idx_hi |= static_cast<uint32_t>(c) << (8 * (g - 4));
+    }
+    __stcs(vals + 2 * q, make_uint4(out[0], out[1], out[2], out[3]));
+    __stcs(vals + 2 * q + 1, make_uint4(out[4], out[5], out[6], out[7]));
+    __stcs(meta + q, code_word);
+    if (idx != nullptr) __stcs(idx + q, make_uint2(idx_lo, idx_hi));
+  }
+}
+
+__global__ void __launch_bounds__(256) decompress_kernel(const uint4* __restrict__ vals,
+                                                         const uint32_t* __restrict__ meta,
+                                                         uint4* __restrict__ W, int64_t items) {
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < items;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 v0 = __ldcs(vals + 2 * q);
+    const uint4 v1 = __ldcs(vals + 2 * q + 1);
+    const uint32_t code_word = __ldcs(meta + q);
+    const uint32_t vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t o[16];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint32_t code = (code_word >> (4 * g)) & 0xFu;
+      const uint32_t i = code & 3u, j = code >> 2;
+      const uint32_t a = vv[g] & 0xFFFFu, b = vv[g] >> 16;
+      uint32_t e[4];
+#pragma unroll
+      for (uint32_t k = 0; k < 4; ++k) e[k] = (k == i) ? a : ((k == j) ? b : 0u);
+      o[2 * g] = e[0] | (e[1] << 16);
+      o[2 * g + 1] = e[2] | (e[3] << 16);
+    }
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      __stcs(W + 4 * q + v, make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]));
+  }
+}
+
+struct NoiseParams {
+  uint4* out;
+  int64_t group_begin;
+  int64_t n;
+  uint32_t step;
+  uint32_t tensor_id;
+  RoundKeys keys;
+};
+
+__global__ void __launch_bounds__(256) noise_words_kernel(const NoiseParams p) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < p.n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    p.out[i] = group_words(static_cast<uint64_t>(p.group_begin + i), p.step, p.tensor_id, p.keys);
+  }
+}
+
+int grid_for(int64_t items, int threads, const Device& d, int per_sm) {
+  const int64_t want = (items + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(per_sm) * d.num_sms;
+  return static_cast<int>(want < cap ? want : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_hard_compress(const Device& d, const uint16_t* W, const float* logits,
+                                 int64_t rows, int64_t cols, uint16_t* values, uint32_t* meta,
+                                 uint8_t* idx, cudaStream_t s) {
+  const int64_t items = rows * cols / 32;
+  hard_compress_kernel<<<grid_for(items, 256, d, 8), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(W), reinterpret_cast<const float4*>(logits),
+      reinterpret_cast<uint4*>(values), meta, reinterpret_cast<uint2*>(idx), items);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decompress(const Device& d, const uint16_t* values, const uint32_t* meta,
+                              int64_t rows, int64_t cols, uint16_t* W_out, cudaStream_t s) {
+  const int64_t items = rows * cols / 32;
+  decompress_kernel<<<grid_for(items, 256, d, 8), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(values), meta, reinterpret_cast<uint4*>(W_out), items);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_noise_words(const Device& d, RngArgs rng, int64_t group_begin, int64_t n,
+                               uint32_t* out4, cudaStream_t s) {
+  NoiseParams p;
+  p.out = reinterpret_cast<uint4*>(out4);
+  p.group_begin = group_begin;
+  p.n = n;
+  p.step = rng.step;
+  p.tensor_id = rng.tensor_id;
+  p.keys = make_round_keys(rng.seed);
+  noise_words_kernel<<<grid_for(n, 256, d, 8), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace maskllm
