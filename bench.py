@@ -51,7 +51,16 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args(argv)
+    ap.add_argument("--only", default=None,
+                    help="comma-separated matrix names of the workload to run (e.g. 'down'); "
+                         "for small profiling runs")
+    ap.add_argument("--kernels", choices=("stream", "direct"), default="stream",
+                    help="stream: pipelined batched kernels; direct: per-matrix kernels with "
+                         "direct vector loads (same results, for comparison)")
+    args = ap.parse_args(argv)
+    if args.kernels == "direct":
+        os.environ["MASKLLM_KERNELS"] = "direct"
+    return args
 
 
 # ---------------------------------------------------------------------------
@@ -215,9 +224,10 @@ def kernel_source_digest() -> str:
 # ---------------------------------------------------------------------------
 
 class Block:
-    """Resident inputs and outputs of one block of matrices on one GPU."""
+    """Resident inputs and outputs of one block of matrices on one GPU, with
+    the C-ABI matrix descriptors built once."""
 
-    def __init__(self, wl, layer, device):
+    def __init__(self, wl, layer, device, only=None):
         import torch
 
         from semi_structured_sparsity_gb300 import binding as mk
@@ -225,45 +235,56 @@ class Block:
         self.mk, self.wl, self.dev = mk, wl, device
         self.mats = []
         for m in range(len(wl.matrices)):
+            if only and wl.matrices[m][0] not in only:
+                continue
             x = W.matrix_inputs(wl, layer, m, device=device)
             if x.L is None:   # logits = magnitude prior + noise
                 x.L = mk.maskllm_prior_init(x.W, wl.prior_scale) + x.L_noise
                 x.L_noise = None
             r, c = x.rows, x.cols
             self.mats.append({
-                "x": x,
-                "L_prior": torch.empty((r, c // 4, 6), dtype=torch.float32, device=device),
+                "x": x, "W": x.W, "logits": x.L, "grad_W_out": x.G, "tensor_id": x.tensor_id,
+                "logits_out": torch.empty((r, c // 4, 6), dtype=torch.float32, device=device),
                 "W_out": torch.empty((r, c), dtype=torch.bfloat16, device=device),
-                "row_sq": torch.empty((r,), dtype=torch.float32, device=device),
-                "dL": torch.empty((r, c // 4, 6), dtype=torch.float32, device=device),
-                "vals": torch.empty((r, c // 2), dtype=torch.bfloat16, device=device),
-                "meta": torch.empty((r, c // 32), dtype=torch.int32, device=device),
+                "row_sq_out": torch.empty((r,), dtype=torch.float32, device=device),
+                "dlogits_out": torch.empty((r, c // 4, 6), dtype=torch.float32, device=device),
+                "values_out": torch.empty((r, c // 2), dtype=torch.bfloat16, device=device),
+                "meta_out": torch.empty((r, c // 32), dtype=torch.int32, device=device),
             })
         torch.cuda.synchronize(device)
+        self.arr = mk.matrix_array(self.mats)
+        self.n = len(self.mats)
         self.weights = sum(m["x"].rows * m["x"].cols for m in self.mats)
+        direct = os.environ.get("MASKLLM_KERNELS") == "direct"
+        per_call = self.n if direct else (self.n + mk.MAX_BATCH - 1) // mk.MAX_BATCH
+        self.launches_per_call = per_call
         self.launches = 0
 
+    def outputs(self, m):
+        return (m["logits_out"], m["W_out"], m["row_sq_out"], m["dlogits_out"], m["values_out"],
+                m["meta_out"])
+
     def run(self, step: int, events=None):
-        """Launch the four kernels over every matrix; events[k] = (start, end)
-        CUDA events bracketing kernel k's launches (optional)."""
-        mk, wl = self.mk, self.wl
+        """One step: each kernel once over all matrices (batched launch);
+        events[k] = (start, end) CUDA events bracketing kernel k (optional)."""
+        import torch
+        mk, wl, L = self.mk, self.wl, self.mk.lib()
+        s = torch.cuda.current_stream(self.dev).cuda_stream
         for k in KERNELS:
             if events is not None:
                 events[k][0].record()
-            for m in self.mats:
-                x = m["x"]
-                rng = (0, step, x.tensor_id)
-                if k == "prior":
-                    mk.maskllm_prior_init(x.W, wl.prior_scale or 1.0, logits_out=m["L_prior"])
-                elif k == "forward":
-                    mk.maskllm_forward(x.W, x.L, wl.tau, wl.kappa, rng, W_out=m["W_out"],
-                                       row_sq_out=m["row_sq"])
-                elif k == "backward":
-                    mk.maskllm_backward(x.W, x.L, x.G, wl.tau, wl.kappa, rng,
-                                        dlogits_out=m["dL"])
-                else:
-                    mk.maskllm_hard_compress(x.W, x.L, values_out=m["vals"], meta_out=m["meta"])
-                self.launches += 1
+            if k == "prior":
+                st = L.maskllm_prior_init_batched(self.arr, self.n, wl.prior_scale or 1.0, s)
+            elif k == "forward":
+                st = L.maskllm_forward_batched(self.arr, self.n, wl.tau, wl.kappa, 0, step, s)
+            elif k == "backward":
+                st = L.maskllm_backward_batched(self.arr, self.n, wl.tau, wl.kappa, 0, step,
+                                                0.0, s)
+            else:
+                st = L.maskllm_hard_compress_batched(self.arr, self.n, s)
+            if st != 0:
+                raise mk.MaskLLMError("maskllm_%s_batched" % k, st)
+            self.launches += self.launches_per_call
             if events is not None:
                 events[k][1].record()
 
@@ -278,7 +299,8 @@ def run_gpu(args):
     dev = torch.device("cuda", ranks.local)
     torch.cuda.set_device(dev)
     wl = W.WORKLOADS[args.workload]
-    blk = Block(wl, layer=ranks.rank % max(wl.layers, 1), device=dev)
+    only = set(args.only.split(",")) if args.only else None
+    blk = Block(wl, layer=ranks.rank % max(wl.layers, 1), device=dev, only=only)
     stream = torch.cuda.current_stream(dev)
 
     for s in range(args.warmup):
@@ -319,8 +341,8 @@ def run_gpu(args):
                       "weights_per_s": blk.weights / per_kernel_s[k],
                       "GB_per_s": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
     dominant = max(KERNELS, key=lambda k: per_kernel_s[k])
-    # per launch = one matrix; report the dominant kernel over the block's
-    # launches: bytes of all its launches over the summed launch time
+    # the dominant kernel's algorithmic bytes over its CUDA-event time (one
+    # batched launch per step covers the whole block)
     ach = BYTES_PER_WEIGHT[dominant] * blk.weights / per_kernel_s[dominant] / 1e9
     tt = traffic_table()
     digest = kernel_source_digest()
@@ -351,8 +373,9 @@ def run_gpu(args):
         "dtype": "bf16 weights, fp32 logits",
         "data": "synthetic (seeded; LLaMA-2-7B block shapes, W~N(0,0.02), logits = magnitude "
                 "prior(300) + N(0,0.1), G~N(0,1e-3))",
-        "config": {"workload": args.workload, "weights_per_gpu": blk.weights,
-                   "matrices": [list(m[1:]) for m in wl.matrices], "tau": wl.tau,
+        "config": {"workload": args.workload + ("[%s]" % args.only if args.only else ""),
+                   "weights_per_gpu": blk.weights,
+                   "matrices": [[m["x"].rows, m["x"].cols] for m in blk.mats], "tau": wl.tau,
                    "kappa": wl.kappa, "parallelism": "dp%d (independent blocks)" % ranks.world,
                    "l2": "inputs larger than L2 (per-kernel sweep reads >= 1.6 GB)"},
         "kernels": kernels,
@@ -360,7 +383,10 @@ def run_gpu(args):
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(ach / peak, 4), "traffic": traffic,
                      "bytes_per_weight": BYTES_PER_WEIGHT[dominant],
-                     "launches_per_step": len(blk.mats)},
+                     "bytes_per_launch": BYTES_PER_WEIGHT[dominant] * blk.weights
+                     / blk.launches_per_call,
+                     "launches_per_step": blk.launches_per_call},
+        "kernel_variant": args.kernels,
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,
@@ -381,8 +407,7 @@ def run_e2e(args, blk, ranks, dev):
         x = m["x"]
         host_in.append([t.cpu().pin_memory() for t in (x.W, x.L, x.G)])
         host_out.append([torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                         for t in (m["L_prior"], m["W_out"], m["row_sq"], m["dL"], m["vals"],
-                                   m["meta"])])
+                         for t in blk.outputs(m)])
     h2d = sum(t.numel() * t.element_size() for h in host_in for t in h)
     d2h = sum(t.numel() * t.element_size() for h in host_out for t in h)
     stream = torch.cuda.current_stream(dev)
@@ -394,8 +419,7 @@ def run_e2e(args, blk, ranks, dev):
                 dst.copy_(src, non_blocking=True)
         blk.run(step)
         for m, hout in zip(blk.mats, host_out):
-            for dst, src in zip(hout, (m["L_prior"], m["W_out"], m["row_sq"], m["dL"],
-                                       m["vals"], m["meta"])):
+            for dst, src in zip(hout, blk.outputs(m)):
                 dst.copy_(src, non_blocking=True)
 
     one(0)

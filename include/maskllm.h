@@ -161,6 +161,61 @@ maskllm_status maskllm_decompress(const uint16_t* values, const uint32_t* meta, 
 maskllm_status maskllm_noise_words(maskllm_rng rng, int64_t group_begin, int64_t n,
                                    uint32_t* out4, maskllm_stream_t stream);
 
+/* ---- Batched calls ------------------------------------------------------
+ * One launch processes up to MASKLLM_MAX_BATCH matrices (for example the
+ * seven linears of a transformer block); longer lists are split into several
+ * launches.  The work of the whole batch is spread over the GPU as one
+ * stream of row chunks, so small matrices do not each pay a launch and a
+ * pipeline ramp.  Per-matrix results are identical to the single-matrix
+ * calls.  Each matrix is described by a maskllm_matrix; a call reads only
+ * the fields of its own operation (the others are ignored), and every rule
+ * of the single-matrix call applies to each matrix.  Outputs may not overlap
+ * any input or output of any matrix in the batch. */
+#define MASKLLM_MAX_BATCH 16
+
+typedef struct {
+  const uint16_t* W;          /* bf16 [rows, cols] (all operations) */
+  const float* logits;        /* fp32 [rows, cols/4, 6] (forward, backward, compress) */
+  const uint16_t* grad_W_out; /* bf16 [rows, cols] (backward) */
+  int64_t rows;
+  int64_t cols;
+  uint32_t tensor_id;         /* noise counter word 3 (forward, backward) */
+  float* logits_out;          /* prior_init output */
+  uint16_t* W_out;            /* forward output */
+  float* row_sq_out;          /* forward output, nullable */
+  float* probs_out;           /* forward output, nullable */
+  float* dlogits_out;         /* backward output */
+  uint16_t* values_out;       /* hard_compress output */
+  uint32_t* meta_out;         /* hard_compress output */
+  uint8_t* idx_out;           /* hard_compress output, nullable */
+} maskllm_matrix;
+
+/* n >= 1 matrices; the noise of matrix i uses (seed, step, mats[i].tensor_id). */
+maskllm_status maskllm_prior_init_batched(const maskllm_matrix* mats, int32_t n, float scale,
+                                          maskllm_stream_t stream);
+maskllm_status maskllm_forward_batched(const maskllm_matrix* mats, int32_t n, float tau,
+                                       float kappa, uint64_t seed, uint32_t step,
+                                       maskllm_stream_t stream);
+maskllm_status maskllm_backward_batched(const maskllm_matrix* mats, int32_t n, float tau,
+                                        float kappa, uint64_t seed, uint32_t step,
+                                        float reg_coeff, maskllm_stream_t stream);
+maskllm_status maskllm_hard_compress_batched(const maskllm_matrix* mats, int32_t n,
+                                             maskllm_stream_t stream);
+
+/* ---- Failure detection -------------------------------------------------
+ * The pipelined kernels wait on shared-memory barriers for their bulk copies.
+ * Every such wait gives up after `nanoseconds` (default 2 s); the kernel then
+ * sets the device error word (see maskllm_device_status), waits up to
+ * max(nanoseconds, 1 s) for its own copies still in flight, and returns.
+ * Applies to launches issued after the call (host-global setting). */
+maskllm_status maskllm_set_wait_timeout(uint64_t nanoseconds);
+
+/* Test hook for the timeout path: while enabled (nonzero), the pipelined
+ * kernels issue no copies at all, so their consumers' waits run out and the
+ * next maskllm_device_status() returns MASKLLM_ERR_TIMEOUT.  Results of
+ * launches issued while enabled are invalid.  Host-global setting. */
+maskllm_status maskllm_test_withhold_loads(int32_t enable);
+
 /* Waits for `stream`, then reads and clears the library's device error word
  * on the current device.  Returns MASKLLM_ERR_TIMEOUT if a bounded wait inside
  * a kernel gave up since the last call (its results are then invalid),

@@ -21,14 +21,26 @@ STATUS = {0: "MASKLLM_OK", 1: "MASKLLM_ERR_INVALID_ARG", 2: "MASKLLM_ERR_SHAPE",
           3: "MASKLLM_ERR_ALIGNMENT", 4: "MASKLLM_ERR_ALIAS", 5: "MASKLLM_ERR_CUDA",
           6: "MASKLLM_ERR_TIMEOUT"}
 
-# The entry points of include/maskllm.h, in declaration order.
+# The entry points of include/maskllm.h.
 EXPORTS = ("maskllm_prior_init", "maskllm_forward", "maskllm_backward",
            "maskllm_hard_compress", "maskllm_decompress", "maskllm_noise_words",
-           "maskllm_device_status", "maskllm_status_string", "maskllm_last_cuda_error")
+           "maskllm_prior_init_batched", "maskllm_forward_batched", "maskllm_backward_batched",
+           "maskllm_hard_compress_batched", "maskllm_set_wait_timeout",
+           "maskllm_test_withhold_loads", "maskllm_device_status", "maskllm_status_string",
+           "maskllm_last_cuda_error")
+MAX_BATCH = 16
 
 
 class maskllm_rng(C.Structure):
     _fields_ = [("seed", C.c_uint64), ("step", C.c_uint32), ("tensor_id", C.c_uint32)]
+
+
+class maskllm_matrix(C.Structure):
+    _fields_ = [("W", C.c_void_p), ("logits", C.c_void_p), ("grad_W_out", C.c_void_p),
+                ("rows", C.c_int64), ("cols", C.c_int64), ("tensor_id", C.c_uint32),
+                ("logits_out", C.c_void_p), ("W_out", C.c_void_p), ("row_sq_out", C.c_void_p),
+                ("probs_out", C.c_void_p), ("dlogits_out", C.c_void_p),
+                ("values_out", C.c_void_p), ("meta_out", C.c_void_p), ("idx_out", C.c_void_p)]
 
 
 class MaskLLMError(RuntimeError):
@@ -57,7 +69,15 @@ def lib() -> C.CDLL:
         L.maskllm_decompress.argtypes = [vp, vp, i64, i64, vp, vp]
         L.maskllm_noise_words.argtypes = [maskllm_rng, i64, i64, vp, vp]
         L.maskllm_device_status.argtypes = [vp]
-        for fn in EXPORTS[:7]:
+        mp = C.POINTER(maskllm_matrix)
+        i32, u64, u32 = C.c_int32, C.c_uint64, C.c_uint32
+        L.maskllm_prior_init_batched.argtypes = [mp, i32, f32, vp]
+        L.maskllm_forward_batched.argtypes = [mp, i32, f32, f32, u64, u32, vp]
+        L.maskllm_backward_batched.argtypes = [mp, i32, f32, f32, u64, u32, f32, vp]
+        L.maskllm_hard_compress_batched.argtypes = [mp, i32, vp]
+        L.maskllm_set_wait_timeout.argtypes = [u64]
+        L.maskllm_test_withhold_loads.argtypes = [i32]
+        for fn in EXPORTS[:-2]:
             getattr(L, fn).restype = st
         L.maskllm_status_string.argtypes = [st]
         L.maskllm_status_string.restype = C.c_char_p
@@ -192,3 +212,64 @@ def maskllm_device_status(stream=None) -> int:
 
 def maskllm_status_string(status: int) -> str:
     return lib().maskllm_status_string(status).decode()
+
+
+# ---------------------------------------------------------------------------
+# Batched calls.  `mats` is a list of dicts with tensor entries named like the
+# fields of maskllm_matrix (W, logits, grad_W_out, logits_out, W_out,
+# row_sq_out, probs_out, dlogits_out, values_out, meta_out, idx_out) and an
+# optional int tensor_id.
+# ---------------------------------------------------------------------------
+
+_TENSOR_FIELDS = ("W", "logits", "grad_W_out", "logits_out", "W_out", "row_sq_out",
+                  "probs_out", "dlogits_out", "values_out", "meta_out", "idx_out")
+
+
+def matrix_array(mats):
+    arr = (maskllm_matrix * len(mats))()
+    for a, m in zip(arr, mats):
+        W = m["W"]
+        if not (isinstance(W, torch.Tensor) and W.is_cuda and W.dtype == torch.bfloat16
+                and W.dim() == 2 and W.is_contiguous()):
+            raise ValueError("W must be a contiguous 2-D bf16 CUDA tensor")
+        a.rows, a.cols = W.shape
+        a.tensor_id = int(m.get("tensor_id", 0))
+        for f in _TENSOR_FIELDS:
+            t = m.get(f)
+            if t is not None:
+                if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+                    raise ValueError("%s must be a contiguous CUDA tensor" % f)
+                setattr(a, f, t.data_ptr())
+    return arr
+
+
+def maskllm_prior_init_batched(mats, scale, stream=None):
+    arr = matrix_array(mats)
+    _check("maskllm_prior_init_batched",
+           lib().maskllm_prior_init_batched(arr, len(mats), scale, _stream(stream)))
+
+
+def maskllm_forward_batched(mats, tau, kappa, seed, step, stream=None):
+    arr = matrix_array(mats)
+    _check("maskllm_forward_batched", lib().maskllm_forward_batched(
+        arr, len(mats), tau, kappa, seed, step, _stream(stream)))
+
+
+def maskllm_backward_batched(mats, tau, kappa, seed, step, reg_coeff=0.0, stream=None):
+    arr = matrix_array(mats)
+    _check("maskllm_backward_batched", lib().maskllm_backward_batched(
+        arr, len(mats), tau, kappa, seed, step, reg_coeff, _stream(stream)))
+
+
+def maskllm_hard_compress_batched(mats, stream=None):
+    arr = matrix_array(mats)
+    _check("maskllm_hard_compress_batched",
+           lib().maskllm_hard_compress_batched(arr, len(mats), _stream(stream)))
+
+
+def maskllm_set_wait_timeout(nanoseconds: int) -> None:
+    _check("maskllm_set_wait_timeout", lib().maskllm_set_wait_timeout(int(nanoseconds)))
+
+
+def maskllm_test_withhold_loads(enable: bool) -> None:
+    _check("maskllm_test_withhold_loads", lib().maskllm_test_withhold_loads(int(bool(enable))))

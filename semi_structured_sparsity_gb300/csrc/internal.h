@@ -40,4 +40,32 @@ cudaError_t launch_noise_words(const Device& d, RngArgs rng, int64_t group_begin
 // s), then clears it.
 cudaError_t read_and_clear_error_word(cudaStream_t s, uint32_t* value);
 
+// ---- pipelined streaming kernels (kernels_stream.cu) ----------------------
+
+constexpr int kMaxBatch = 16;   // matrices per launch
+
+struct StreamMatrix {
+  const void* W;      // bf16 [rows, cols]
+  const void* L;      // fp32 [rows, cols/4, 6]
+  const void* G;      // bf16 [rows, cols] (backward)
+  void* out0;         // prior: logits; forward: W'; backward: dlogits; compress: values
+  void* out1;         // forward: row_sq (nullable); compress: codes
+  void* out2;         // forward: probs (nullable); compress: idx (nullable)
+  int64_t rows;
+  int64_t cols;
+  uint32_t tensor_id;
+};
+
+cudaError_t stream_prior_init(const Device& d, const StreamMatrix* m, int n, float scale,
+                              cudaStream_t s);
+cudaError_t stream_forward(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
+                           RngArgs rng, bool probs, cudaStream_t s);
+cudaError_t stream_backward(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
+                            RngArgs rng, float reg_coeff, cudaStream_t s);
+cudaError_t stream_hard_compress(const Device& d, const StreamMatrix* m, int n, cudaStream_t s);
+void stream_set_wait_ns(uint64_t ns);
+uint64_t stream_wait_ns();
+void stream_set_withhold_loads(int on);
+cudaError_t read_and_clear_stream_error(cudaStream_t s, uint32_t* value);
+
 }  // namespace maskllm

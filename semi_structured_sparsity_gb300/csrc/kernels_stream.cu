@@ -1,0 +1,750 @@
+// kernels_stream.cu -- the four hot-path kernels as persistent, bulk-copy
+// pipelined streams over a batch of matrices.
+//
+// "MaskLLM: Learnable Semi-Structured Sparsity for Large Language Models",
+// Fig. 3 (Gumbel-softmax draw over the 2:4 candidates of every group of four,
+// weighted average of the candidate masks, all differentiable), Fig. 5
+// (kappa), Table 2 (prior masks), Table 3 (weight regularisation);
+// "Accelerating Sparse Deep Neural Networks", Sec. 3.1 (compressed 2:4
+// storage) and Sec. 4.1 (magnitude pruning).
+//
+// Structure (one CTA per SM, 1 producer warp + 16 consumer warps):
+//   * Work is a list of chunks.  A chunk is up to 1024 consecutive groups of
+//     one row, or several whole short rows (<= 1024 groups).  The chunks of a
+//     launch are those of up to 16 matrices, concatenated; CTA b takes a
+//     contiguous range of them, cut at row boundaries, so every row is
+//     finished inside one CTA (its sum of squares needs no cross-CTA step)
+//     and the CTAs carry equal byte counts to within one row.
+//   * The producer warp copies each chunk's inputs (W: 8 bytes per group,
+//     logits: 24, upstream gradient: 8) from global into one of 4 shared
+//     stages with bulk copies completing on the stage's "full" mbarrier.
+//   * Consumer thread t owns groups 2t and 2t+1 of every chunk: it reads them
+//     from shared memory, computes, and either stores its results straight to
+//     global memory (16-byte coalesced stores) or writes them back into the
+//     stage, from where the producer bulk-stores the whole chunk.  Each
+//     consumer warp then arrives on the stage's "empty" mbarrier.
+//   * After a stage's empty barrier completes, the producer finishes that
+//     chunk: it sums the per-thread row partials in a fixed order (forward)
+//     and issues the bulk store of staged outputs, then refills the stage.
+//   * Every wait is bounded (pipeline.cuh).  On a timeout the CTA raises an
+//     abort flag, sets the device error word, the producer waits (bounded)
+//     for its copies still in flight, and all warps return.
+#include "device_common.cuh"
+#include "internal.h"
+#include "pipeline.cuh"
+
+namespace maskllm {
+
+__device__ __align__(16) float g_gumbel_table_s[kTableSize] = {
+#include "gumbel_table.inc"
+};
+
+// Bit 0: a consumer wait timed out; bit 1: a producer wait timed out;
+// bit 2: the final drain of in-flight copies timed out.
+__device__ uint32_t g_stream_error_word = 0;
+
+namespace {
+
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kChunkGroups = 2 * kConsumers;  // 1024
+constexpr int kStages = 4;
+constexpr int kMaxMats = kMaxBatch;
+
+struct MatDesc {
+  const void* W;          // bf16 [rows, cols]
+  const void* L;          // fp32 [rows, cols/4, 6]
+  const void* G;          // bf16 [rows, cols] (backward)
+  void* out0;             // prior: logits; forward: W'; backward: dlogits; compress: values
+  void* out1;             // forward: row_sq; compress: codes
+  void* out2;             // forward: probs; compress: idx
+  int64_t rows;
+  int64_t unit_begin;     // first unit of this matrix in the launch's unit list
+  int64_t chunk_begin;    // first chunk of this matrix in the launch's chunk list
+  int32_t gpr;            // groups per row (cols / 4)
+  int32_t cpr;            // chunks per row when a row spans >= 1 chunk, else 0
+  int32_t rpc;            // rows per chunk when rows are short, else 0
+  uint32_t tensor_id;
+};
+
+struct Scalars {
+  float kappa;
+  float rho;
+  float dz_dlogit;
+  float two_reg;
+  float scale;
+  uint32_t step;
+  RoundKeys keys;
+};
+
+struct StreamParams {
+  MatDesc mats[kMaxMats];
+  int32_t nmats;
+  int64_t total_units;
+  int64_t total_chunks;
+  uint64_t wait_ns;        // bound of every pipeline wait
+  uint64_t drain_ns;       // bound of the final wait for copies in flight
+  int32_t withhold_loads;  // test hook: the producer issues no copies
+  Scalars s;
+};
+
+struct Chunk {
+  int32_t mat;
+  int32_t ng;       // groups in the chunk
+  int64_t g0;       // first group, matrix-local
+  int64_t row0;     // first row
+  int32_t nrows;    // whole rows ending in this chunk (0 when a long row continues)
+};
+
+__device__ __forceinline__ int64_t units_of(const MatDesc& d) {
+  return d.cpr > 0 ? d.rows : (d.rows + d.rpc - 1) / d.rpc;
+}
+
+// Walks the chunks of units [u, u_end) of the launch's unit list.
+struct ChunkIter {
+  const StreamParams* p;
+  int32_t m;
+  int64_t lu;       // unit within matrix m
+  int32_t j;        // chunk within the unit (long rows)
+  int64_t left;     // units left
+
+  __device__ void init(const StreamParams* pp, int64_t u, int64_t u_end) {
+    p = pp;
+    left = u_end - u;
+    m = 0;
+    while (m + 1 < p->nmats && p->mats[m + 1].unit_begin <= u) ++m;
+    lu = u - p->mats[m].unit_begin;
+    j = 0;
+  }
+
+  __device__ bool next(Chunk& c) {
+    if (left <= 0) return false;
+    const MatDesc& d = p->mats[m];
+    c.mat = m;
+    if (d.cpr > 0) {
+      c.row0 = lu;
+      c.g0 = lu * d.gpr + static_cast<int64_t>(j) * kChunkGroups;
+      const int64_t rest = d.gpr - static_cast<int64_t>(j) * kChunkGroups;
+      c.ng = static_cast<int32_t>(rest < kChunkGroups ? rest : kChunkGroups);
+      const bool last = (j + 1 == d.cpr);
+      c.nrows = last ? 1 : 0;
+      if (last) {
+        j = 0;
+        ++lu;
+        --left;
+      } else {
+        ++j;
+      }
+    } else {
+      c.row0 = lu * d.rpc;
+      const int64_t r_rest = d.rows - c.row0;
+      c.nrows = static_cast<int32_t>(r_rest < d.rpc ? r_rest : d.rpc);
+      c.g0 = c.row0 * d.gpr;
+      c.ng = c.nrows * d.gpr;
+      ++lu;
+      --left;
+    }
+    if (lu >= units_of(d) && left > 0) {
+      ++m;
+      lu = 0;
+      j = 0;
+    }
+    return true;
+  }
+};
+
+// First unit of CTA b: the unit boundary at or after chunk total*b/G.
+__device__ int64_t cta_first_unit(const StreamParams& p, int64_t b, int64_t G) {
+  if (b >= G) return p.total_units;
+  const int64_t target = p.total_chunks * b / G;   // total_chunks < 2^44, b < 2^16
+  int m = 0;
+  while (m + 1 < p.nmats && p.mats[m + 1].chunk_begin <= target) ++m;
+  const MatDesc& d = p.mats[m];
+  const int64_t t = target - d.chunk_begin;
+  const int64_t per_unit = d.cpr > 0 ? d.cpr : 1;
+  int64_t u = (t + per_unit - 1) / per_unit;
+  const int64_t nu = units_of(d);
+  if (u > nu) u = nu;
+  return d.unit_begin + u;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag, uint32_t bit) {
+  *abort_flag = 1;
+  atomicOr(&g_stream_error_word, bit);
+}
+
+// ---------------------------------------------------------------------------
+// Per-op policies.
+//   kTable      the Gumbel table is loaded into shared memory
+//   kRowSq      consumers leave per-thread row partials for the producer
+//   kStaged     consumers write the chunk's output into the stage; the
+//               producer bulk-stores it (kOutBytesPerGroup bytes per group
+//               from stage offset kOutOffset to out0)
+// ---------------------------------------------------------------------------
+
+struct PriorOp {
+  static constexpr bool kTable = false, kRowSq = false, kStaged = true, kWarpWide = false;
+  static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
+  static constexpr uint32_t kOutOffset = kChunkGroups * 8;
+  static constexpr uint32_t kOutBytesPerGroup = 24;
+
+  __device__ static uint32_t issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
+    const uint32_t wb = static_cast<uint32_t>(c.ng) * 8;
+    mbar_arrive_expect_tx(bar, wb);
+    bulk_load(st, static_cast<const uint8_t*>(d.W) + c.g0 * 8, wb, bar);
+    return wb;
+  }
+
+  __device__ static void consume(const StreamParams& p, const MatDesc&, const Chunk&, uint8_t* st,
+                                 int t, const float*, float&, float*) {
+    const uint4 w = *reinterpret_cast<const uint4*>(st + 16 * t);
+    float a[kCand], b[kCand];
+    const float s = p.s.scale;
+    const float w0 = fabsf(bf16_lo(w.x)), w1 = fabsf(bf16_hi(w.x));
+    const float w2 = fabsf(bf16_lo(w.y)), w3 = fabsf(bf16_hi(w.y));
+    const float w4 = fabsf(bf16_lo(w.z)), w5 = fabsf(bf16_hi(w.z));
+    const float w6 = fabsf(bf16_lo(w.w)), w7 = fabsf(bf16_hi(w.w));
+    a[0] = __fmul_rn(s, __fadd_rn(w0, w1));
+    a[1] = __fmul_rn(s, __fadd_rn(w0, w2));
+    a[2] = __fmul_rn(s, __fadd_rn(w0, w3));
+    a[3] = __fmul_rn(s, __fadd_rn(w1, w2));
+    a[4] = __fmul_rn(s, __fadd_rn(w1, w3));
+    a[5] = __fmul_rn(s, __fadd_rn(w2, w3));
+    b[0] = __fmul_rn(s, __fadd_rn(w4, w5));
+    b[1] = __fmul_rn(s, __fadd_rn(w4, w6));
+    b[2] = __fmul_rn(s, __fadd_rn(w4, w7));
+    b[3] = __fmul_rn(s, __fadd_rn(w5, w6));
+    b[4] = __fmul_rn(s, __fadd_rn(w5, w7));
+    b[5] = __fmul_rn(s, __fadd_rn(w6, w7));
+    float4* o = reinterpret_cast<float4*>(st + kOutOffset + 48 * t);
+    o[0] = make_float4(a[0], a[1], a[2], a[3]);
+    o[1] = make_float4(a[4], a[5], b[0], b[1]);
+    o[2] = make_float4(b[2], b[3], b[4], b[5]);
+  }
+};
+
+template <bool kProbs>
+struct FwdOp {
+  static constexpr bool kTable = true, kRowSq = true, kStaged = false, kWarpWide = false;
+  static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
+  static constexpr uint32_t kOutOffset = 0;
+  static constexpr uint32_t kOutBytesPerGroup = 0;
+
+  __device__ static uint32_t issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
+    const uint32_t wb = static_cast<uint32_t>(c.ng) * 8, lb = static_cast<uint32_t>(c.ng) * 24;
+    mbar_arrive_expect_tx(bar, wb + lb);
+    bulk_load(st, static_cast<const uint8_t*>(d.W) + c.g0 * 8, wb, bar);
+    bulk_load(st + kChunkGroups * 8, static_cast<const uint8_t*>(d.L) + c.g0 * 24, lb, bar);
+    return wb + lb;
+  }
+
+  __device__ static void group(const StreamParams& p, const float* tab, uint64_t gidx,
+                               uint32_t tensor_id, const float L[kCand], uint32_t w01,
+                               uint32_t w23, uint32_t& o01, uint32_t& o23, float& acc,
+                               float prob[kCand]) {
+    float g[kCand], e[kCand], inv, M[4];
+    gumbel6(group_words(gidx, p.s.step, tensor_id, p.s.keys), tab, g);
+    softmax6(L, g, p.s.kappa, p.s.rho, e, inv);
+    soft_mask4(e, inv, M);
+    const float x0 = __fmul_rn(bf16_lo(w01), M[0]);
+    const float x1 = __fmul_rn(bf16_hi(w01), M[1]);
+    const float x2 = __fmul_rn(bf16_lo(w23), M[2]);
+    const float x3 = __fmul_rn(bf16_hi(w23), M[3]);
+    o01 = pack_bf16x2_rn(x0, x1);
+    o23 = pack_bf16x2_rn(x2, x3);
+    acc = __fmaf_rn(x0, x0, acc);
+    acc = __fmaf_rn(x1, x1, acc);
+    acc = __fmaf_rn(x2, x2, acc);
+    acc = __fmaf_rn(x3, x3, acc);
+    if (kProbs) {
+#pragma unroll
+      for (int c = 0; c < kCand; ++c) prob[c] = e[c] * inv;
+    }
+  }
+
+  __device__ static void consume(const StreamParams& p, const MatDesc& d, const Chunk& c,
+                                 uint8_t* st, int t, const float* tab, float& acc,
+                                 float* part) {
+    const int64_t item = c.g0 / 2 + t;
+    const uint4 w = *reinterpret_cast<const uint4*>(st + 16 * t);
+    const float4* Ls = reinterpret_cast<const float4*>(st + kChunkGroups * 8 + 48 * t);
+    const float4 a = Ls[0], b = Ls[1], cc = Ls[2];
+    const float La[kCand] = {a.x, a.y, a.z, a.w, b.x, b.y};
+    const float Lb[kCand] = {b.z, b.w, cc.x, cc.y, cc.z, cc.w};
+    uint4 o;
+    float pa[kCand], pb[kCand];
+    group(p, tab, 2 * static_cast<uint64_t>(item), d.tensor_id, La, w.x, w.y, o.x, o.y, acc, pa);
+    group(p, tab, 2 * static_cast<uint64_t>(item) + 1, d.tensor_id, Lb, w.z, w.w, o.z, o.w, acc,
+          pb);
+    __stcs(static_cast<uint4*>(d.out0) + item, o);
+    if (kProbs && d.out2 != nullptr) {
+      float4* q = static_cast<float4*>(d.out2) + 3 * item;
+      q[0] = make_float4(pa[0], pa[1], pa[2], pa[3]);
+      q[1] = make_float4(pa[4], pa[5], pb[0], pb[1]);
+      q[2] = make_float4(pb[2], pb[3], pb[4], pb[5]);
+    }
+    (void)part;
+  }
+};
+
+template <bool kReg>
+struct BwdOp {
+  static constexpr bool kTable = true, kRowSq = false, kStaged = true, kWarpWide = false;
+  static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 8 + 24);
+  static constexpr uint32_t kOutOffset = kChunkGroups * 16;
+  static constexpr uint32_t kOutBytesPerGroup = 24;
+
+  __device__ static uint32_t issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
+    const uint32_t wb = static_cast<uint32_t>(c.ng) * 8, lb = static_cast<uint32_t>(c.ng) * 24;
+    mbar_arrive_expect_tx(bar, 2 * wb + lb);
+    bulk_load(st, static_cast<const uint8_t*>(d.W) + c.g0 * 8, wb, bar);
+    bulk_load(st + kChunkGroups * 8, static_cast<const uint8_t*>(d.G) + c.g0 * 8, wb, bar);
+    bulk_load(st + kChunkGroups * 16, static_cast<const uint8_t*>(d.L) + c.g0 * 24, lb, bar);
+    return 2 * wb + lb;
+  }
+
+  __device__ static void group(const StreamParams& p, const float* tab, uint64_t gidx,
+                               uint32_t tensor_id, const float L[kCand], uint32_t w01,
+                               uint32_t w23, uint32_t g01, uint32_t g23, float out[kCand]) {
+    float g[kCand], e[kCand], inv;
+    gumbel6(group_words(gidx, p.s.step, tensor_id, p.s.keys), tab, g);
+    softmax6(L, g, p.s.kappa, p.s.rho, e, inv);
+    const float w[4] = {bf16_lo(w01), bf16_hi(w01), bf16_lo(w23), bf16_hi(w23)};
+    float t[4] = {bf16_lo(g01), bf16_hi(g01), bf16_lo(g23), bf16_hi(g23)};
+    if (kReg) {
+      float M[4];
+      soft_mask4(e, inv, M);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) t[j] = __fmaf_rn(p.s.two_reg, __fmul_rn(w[j], M[j]), t[j]);
+    }
+    float h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = t[j] * w[j];
+    const float dp[kCand] = {h[0] + h[1], h[0] + h[2], h[0] + h[3],
+                             h[1] + h[2], h[1] + h[3], h[2] + h[3]};
+    float pr[kCand];
+    float r = 0.f;
+#pragma unroll
+    for (int c = 0; c < kCand; ++c) {
+      pr[c] = e[c] * inv;
+      r = __fmaf_rn(pr[c], dp[c], r);
+    }
+#pragma unroll
+    for (int c = 0; c < kCand; ++c) out[c] = (p.s.dz_dlogit * pr[c]) * (dp[c] - r);
+  }
+
+  __device__ static void consume(const StreamParams& p, const MatDesc& d, const Chunk& c,
+                                 uint8_t* st, int t, const float* tab, float&, float*) {
+    const int64_t item = c.g0 / 2 + t;
+    const uint4 w = *reinterpret_cast<const uint4*>(st + 16 * t);
+    const uint4 gr = *reinterpret_cast<const uint4*>(st + kChunkGroups * 8 + 16 * t);
+    float4* Ls = reinterpret_cast<float4*>(st + kChunkGroups * 16 + 48 * t);
+    const float4 a = Ls[0], b = Ls[1], cc = Ls[2];
+    const float La[kCand] = {a.x, a.y, a.z, a.w, b.x, b.y};
+    const float Lb[kCand] = {b.z, b.w, cc.x, cc.y, cc.z, cc.w};
+    float da[kCand], db[kCand];
+    group(p, tab, 2 * static_cast<uint64_t>(item), d.tensor_id, La, w.x, w.y, gr.x, gr.y, da);
+    group(p, tab, 2 * static_cast<uint64_t>(item) + 1, d.tensor_id, Lb, w.z, w.w, gr.z, gr.w, db);
+    // dlogits overwrite this thread's own logits in the stage
+    Ls[0] = make_float4(da[0], da[1], da[2], da[3]);
+    Ls[1] = make_float4(da[4], da[5], db[0], db[1]);
+    Ls[2] = make_float4(db[2], db[3], db[4], db[5]);
+  }
+};
+
+// Candidate c's kept positions and metadata code, one nibble per candidate:
+// c0 (0,1) c1 (0,2) c2 (0,3) c3 (1,2) c4 (1,3) c5 (2,3).
+constexpr uint32_t kPairI = 0x211000u;
+constexpr uint32_t kPairJ = 0x332321u;
+constexpr uint32_t kCode = 0xED9C84u;
+
+__device__ __forceinline__ int first_argmax6(const float L[kCand]) {
+  int best = 0;
+  float bv = L[0];
+  bool bnan = isnan(L[0]);
+#pragma unroll
+  for (int c = 1; c < kCand; ++c) {
+    if (!isnan(L[c]) && (bnan || L[c] > bv)) {
+      best = c;
+      bv = L[c];
+      bnan = false;
+    }
+  }
+  return best;
+}
+
+__device__ __forceinline__ uint32_t select4(uint32_t e0, uint32_t e1, uint32_t e2, uint32_t e3,
+                                            uint32_t k) {
+  return k == 0 ? e0 : (k == 1 ? e1 : (k == 2 ? e2 : e3));
+}
+
+struct CompressOp {
+  static constexpr bool kTable = false, kRowSq = false, kStaged = false, kWarpWide = true;
+  static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
+  static constexpr uint32_t kOutOffset = 0;
+  static constexpr uint32_t kOutBytesPerGroup = 0;
+
+  __device__ static uint32_t issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
+    return FwdOp<false>::issue(d, c, st, bar);
+  }
+
+  // Kept pair of one group: returns (w_i | w_j << 16) and sets the code.
+  __device__ static uint32_t keep(const float L[kCand], uint32_t w01, uint32_t w23, uint32_t& code,
+                                  uint32_t& cand) {
+    const int c = first_argmax6(L);
+    const uint32_t i = (kPairI >> (4 * c)) & 0xFu, j = (kPairJ >> (4 * c)) & 0xFu;
+    const uint32_t e0 = w01 & 0xFFFFu, e1 = w01 >> 16, e2 = w23 & 0xFFFFu, e3 = w23 >> 16;
+    code = (kCode >> (4 * c)) & 0xFu;
+    cand = static_cast<uint32_t>(c);
+    return select4(e0, e1, e2, e3, i) | (select4(e0, e1, e2, e3, j) << 16);
+  }
+
+  __device__ static void consume(const StreamParams&, const MatDesc& d, const Chunk& c,
+                                 uint8_t* st, int t, const float*, float&, float*) {
+    // all 32 lanes of a warp take this path together (chunks hold a multiple
+    // of 8 groups, so the 4 lanes sharing a code word are all active or not)
+    const int64_t item = c.g0 / 2 + t;
+    const bool active = 2 * t < c.ng;
+    uint32_t byte = 0;
+    if (active) {
+      const uint4 w = *reinterpret_cast<const uint4*>(st + 16 * t);
+      const float4* Ls = reinterpret_cast<const float4*>(st + kChunkGroups * 8 + 48 * t);
+      const float4 a = Ls[0], b = Ls[1], cc = Ls[2];
+      const float La[kCand] = {a.x, a.y, a.z, a.w, b.x, b.y};
+      const float Lb[kCand] = {b.z, b.w, cc.x, cc.y, cc.z, cc.w};
+      uint32_t ca, cb, ka, kb;
+      const uint32_t va = keep(La, w.x, w.y, ca, ka);
+      const uint32_t vb = keep(Lb, w.z, w.w, cb, kb);
+      __stcs(static_cast<uint2*>(d.out0) + item, make_uint2(va, vb));
+      byte = ca | (cb << 4);
+      if (d.out2 != nullptr)
+        static_cast<uint16_t*>(d.out2)[item] = static_cast<uint16_t>(ka | (kb << 8));
+    }
+    // four consecutive lanes hold the 8 codes of one 32-bit metadata word
+    const int lane = t & 31;
+    uint32_t word = byte << (8 * (lane & 3));
+    word |= __shfl_down_sync(0xFFFFFFFFu, word, 1);
+    word |= __shfl_down_sync(0xFFFFFFFFu, word, 2);
+    if (active && (lane & 3) == 0) __stcs(static_cast<uint32_t*>(d.out1) + item / 4, word);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// ---------------------------------------------------------------------------
+
+template <class Op>
+struct Layout {
+  static constexpr uint32_t kTableBytes = Op::kTable ? kTableSize * 4 : 0;
+  static constexpr uint32_t kStageOff = kTableBytes;
+  static constexpr uint32_t kPartOff = kStageOff + kStages * Op::kStageBytes;
+  static constexpr uint32_t kPartBytes = Op::kRowSq ? kStages * kConsumers * 4 : 0;
+  static constexpr uint32_t kBarOff = kPartOff + kPartBytes;
+  static constexpr uint32_t kChunkOff = kBarOff + 2 * kStages * 8;
+  static constexpr uint32_t kFlagOff = kChunkOff + kStages * sizeof(Chunk);
+  static constexpr uint32_t kBytes = kFlagOff + 16;
+};
+
+template <class Op>
+__device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64_t u1) {
+  using Lay = Layout<Op>;
+  const int lane = threadIdx.x & 31;
+  uint8_t* stages = smem + Lay::kStageOff;
+  const float* part = reinterpret_cast<const float*>(smem + Lay::kPartOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
+  uint64_t* empty = full + kStages;
+  Chunk* held = reinterpret_cast<Chunk*>(smem + Lay::kChunkOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kFlagOff);
+
+  // Finish the chunk that occupied stage s: row sums and staged stores.
+  auto retire = [&](int s) {
+    const Chunk c = held[s];
+    const MatDesc& d = p.mats[c.mat];
+    if (Op::kRowSq && d.out1 != nullptr && c.nrows > 0) {
+      const float* ps = part + s * kConsumers;
+      float* row_sq = static_cast<float*>(d.out1);
+      if (d.cpr > 0) {
+        float v = 0.f;
+        for (int k = lane; k < kConsumers; k += 32) v += ps[k];
+        v = warp_sum(v);
+        if (lane == 0) row_sq[c.row0] = v;
+      } else {
+        const int ipr = d.gpr / 2;
+        for (int r = 0; r < c.nrows; ++r) {
+          float v = 0.f;
+          for (int k = lane; k < ipr; k += 32) v += ps[r * ipr + k];
+          v = warp_sum(v);
+          if (lane == 0) row_sq[c.row0 + r] = v;
+        }
+      }
+    }
+    if (Op::kStaged && lane == 0) {
+      bulk_store(static_cast<uint8_t*>(d.out0) + c.g0 * Op::kOutBytesPerGroup,
+                 stages + s * Op::kStageBytes + Op::kOutOffset,
+                 static_cast<uint32_t>(c.ng) * Op::kOutBytesPerGroup);
+      bulk_commit();
+    }
+  };
+
+  ChunkIter it;
+  it.init(&p, u0, u1);
+  Chunk c;
+  int64_t n = 0;
+  bool ok = true;
+  while (ok && it.next(c)) {
+    const int s = static_cast<int>(n % kStages);
+    if (n >= kStages) {
+      const bool got = mbar_wait_bounded(&empty[s], static_cast<uint32_t>((n / kStages - 1) & 1),
+                                         p.wait_ns, abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, got)) {
+        if (lane == 0) raise_abort(abort_flag, 2u);
+        ok = false;
+        break;
+      }
+      retire(s);
+      __syncwarp();
+      if (Op::kStaged && lane == 0) bulk_wait_reads();  // stage s is about to be refilled
+    }
+    if (lane == 0) held[s] = c;
+    __syncwarp();
+    if (lane == 0 && !p.withhold_loads) Op::issue(p.mats[c.mat], c, stages + s * Op::kStageBytes,
+                                                  &full[s]);
+    ++n;
+  }
+  if (ok) {
+    // drain: finish the last chunks as their consumers release them
+    const int64_t first = n > kStages ? n - kStages : 0;
+    for (int64_t k = first; k < n; ++k) {
+      const int s = static_cast<int>(k % kStages);
+      const bool got = mbar_wait_bounded(&empty[s], static_cast<uint32_t>((k / kStages) & 1),
+                                         p.wait_ns, abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, got)) {
+        if (lane == 0) raise_abort(abort_flag, 2u);
+        ok = false;
+        break;
+      }
+      retire(s);
+      __syncwarp();
+    }
+  }
+  if (!ok && !p.withhold_loads) {
+    // aborted: wait (bounded) for every copy still landing in shared memory
+    const int64_t first = n > kStages ? n - kStages : 0;
+    for (int64_t k = first; k < n; ++k) {
+      const int s = static_cast<int>(k % kStages);
+      int never = 0;
+      if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((k / kStages) & 1), p.drain_ns,
+                             &never)) {
+        if (lane == 0) atomicOr(&g_stream_error_word, 4u);
+      }
+    }
+  }
+  if (Op::kStaged && lane == 0) bulk_wait_all();
+}
+
+template <class Op>
+__device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64_t u1) {
+  using Lay = Layout<Op>;
+  const int t = threadIdx.x - 32;
+  const int lane = threadIdx.x & 31;
+  uint8_t* stages = smem + Lay::kStageOff;
+  float* part = reinterpret_cast<float*>(smem + Lay::kPartOff);
+  const float* tab = reinterpret_cast<const float*>(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
+  uint64_t* empty = full + kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kFlagOff);
+
+  ChunkIter it;
+  it.init(&p, u0, u1);
+  Chunk c;
+  int64_t n = 0;
+  float acc = 0.f;
+  while (it.next(c)) {
+    const int s = static_cast<int>(n % kStages);
+    const bool got = mbar_wait_bounded(&full[s], static_cast<uint32_t>((n / kStages) & 1),
+                                       p.wait_ns, abort_flag);
+    if (!__all_sync(0xFFFFFFFFu, got)) {
+      if (lane == 0) raise_abort(abort_flag, 1u);
+      break;
+    }
+    const MatDesc& d = p.mats[c.mat];
+    uint8_t* st = stages + s * Op::kStageBytes;
+    if (Op::kWarpWide)
+      Op::consume(p, d, c, st, t, tab, acc, part);   // every lane, active or not
+    else if (2 * t < c.ng)
+      Op::consume(p, d, c, st, t, tab, acc, part);
+    if (Op::kRowSq) {
+      float* ps = part + s * kConsumers;
+      if (d.cpr > 0) {
+        if (c.nrows > 0) {
+          ps[t] = acc;   // the row ends in this chunk
+          acc = 0.f;
+        }
+      } else {
+        ps[t] = acc;     // short rows: one item per thread per chunk
+        acc = 0.f;
+      }
+    }
+    if (Op::kStaged) fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    ++n;
+  }
+}
+
+template <class Op>
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ StreamParams p) {
+  using Lay = Layout<Op>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  if (Op::kTable) {
+    const float4* src = reinterpret_cast<const float4*>(g_gumbel_table_s);
+    float4* dst = reinterpret_cast<float4*>(smem);
+    for (int i = threadIdx.x; i < kTableSize / 4; i += kThreads) dst[i] = src[i];
+  }
+  if (threadIdx.x == 0) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars[s], 1);                           // full: producer's expect_tx
+      mbar_init(&bars[kStages + s], kConsumerWarps);    // empty: one arrive per consumer warp
+    }
+    *reinterpret_cast<volatile int*>(smem + Lay::kFlagOff) = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int64_t u0 = cta_first_unit(p, blockIdx.x, gridDim.x);
+  const int64_t u1 = cta_first_unit(p, blockIdx.x + 1, gridDim.x);
+  if (threadIdx.x < 32)
+    producer<Op>(p, smem, u0, u1);
+  else
+    consumer<Op>(p, smem, u0, u1);
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+
+uint64_t g_wait_ns = 2000000000ull;   // 2 s
+int g_withhold_loads = 0;
+
+void describe(StreamParams& p, const StreamMatrix* mats, int n) {
+  p.nmats = n;
+  int64_t units = 0, chunks = 0;
+  for (int i = 0; i < n; ++i) {
+    MatDesc& d = p.mats[i];
+    const StreamMatrix& m = mats[i];
+    d.W = m.W;
+    d.L = m.L;
+    d.G = m.G;
+    d.out0 = m.out0;
+    d.out1 = m.out1;
+    d.out2 = m.out2;
+    d.rows = m.rows;
+    d.gpr = static_cast<int32_t>(m.cols / 4);
+    d.tensor_id = m.tensor_id;
+    if (d.gpr >= kChunkGroups) {
+      d.cpr = (d.gpr + kChunkGroups - 1) / kChunkGroups;
+      d.rpc = 0;
+    } else {
+      d.cpr = 0;
+      d.rpc = kChunkGroups / d.gpr;
+    }
+    d.unit_begin = units;
+    d.chunk_begin = chunks;
+    const int64_t u = d.cpr > 0 ? d.rows : (d.rows + d.rpc - 1) / d.rpc;
+    units += u;
+    chunks += d.cpr > 0 ? u * d.cpr : u;
+  }
+  p.total_units = units;
+  p.total_chunks = chunks;
+  p.wait_ns = g_wait_ns;
+  p.drain_ns = g_wait_ns > 1000000000ull ? g_wait_ns : 1000000000ull;
+  p.withhold_loads = g_withhold_loads;
+}
+
+template <class Op>
+cudaError_t launch(const Device& dev, const StreamParams& p, cudaStream_t s) {
+  const uint32_t bytes = Layout<Op>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(stream_kernel<Op>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = p.total_units < dev.num_sms ? p.total_units : dev.num_sms;
+  stream_kernel<Op><<<static_cast<int>(grid), kThreads, bytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+Scalars scalars(float tau, float kappa, RngArgs rng, float reg, float scale) {
+  Scalars sc;
+  sc.kappa = kappa;
+  sc.rho = static_cast<float>(1.0 / static_cast<double>(tau));
+  sc.dz_dlogit = static_cast<float>(static_cast<double>(kappa) * static_cast<double>(sc.rho));
+  sc.two_reg = 2.0f * reg;
+  sc.scale = scale;
+  sc.step = rng.step;
+  sc.keys = make_round_keys(rng.seed);
+  return sc;
+}
+
+}  // namespace
+
+static_assert(Layout<FwdOp<true>>::kBytes <= 232448, "forward shared memory");
+static_assert(Layout<BwdOp<true>>::kBytes <= 232448, "backward shared memory");
+static_assert(sizeof(StreamParams) <= 4000, "kernel parameters");
+
+cudaError_t stream_prior_init(const Device& d, const StreamMatrix* m, int n, float scale,
+                              cudaStream_t s) {
+  StreamParams p;
+  describe(p, m, n);
+  p.s = scalars(1.0f, 0.0f, {0, 0, 0}, 0.0f, scale);
+  return launch<PriorOp>(d, p, s);
+}
+
+cudaError_t stream_forward(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
+                           RngArgs rng, bool probs, cudaStream_t s) {
+  StreamParams p;
+  describe(p, m, n);
+  p.s = scalars(tau, kappa, rng, 0.0f, 0.0f);
+  return probs ? launch<FwdOp<true>>(d, p, s) : launch<FwdOp<false>>(d, p, s);
+}
+
+cudaError_t stream_backward(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
+                            RngArgs rng, float reg_coeff, cudaStream_t s) {
+  StreamParams p;
+  describe(p, m, n);
+  p.s = scalars(tau, kappa, rng, reg_coeff, 0.0f);
+  return reg_coeff != 0.0f ? launch<BwdOp<true>>(d, p, s) : launch<BwdOp<false>>(d, p, s);
+}
+
+cudaError_t stream_hard_compress(const Device& d, const StreamMatrix* m, int n, cudaStream_t s) {
+  StreamParams p;
+  describe(p, m, n);
+  p.s = scalars(1.0f, 0.0f, {0, 0, 0}, 0.0f, 0.0f);
+  return launch<CompressOp>(d, p, s);
+}
+
+void stream_set_wait_ns(uint64_t ns) { g_wait_ns = ns; }
+uint64_t stream_wait_ns() { return g_wait_ns; }
+void stream_set_withhold_loads(int on) { g_withhold_loads = on; }
+
+cudaError_t read_and_clear_stream_error(cudaStream_t s, uint32_t* value) {
+  uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(value, g_stream_error_word, sizeof(uint32_t), 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+  if (*value != 0) {
+    e = cudaMemcpyToSymbolAsync(g_stream_error_word, &zero, sizeof(uint32_t), 0,
+                                cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+  }
+  return e;
+}
+
+}  // namespace maskllm

@@ -1,8 +1,15 @@
 // maskllm_api.cu -- the C ABI declared in include/maskllm.h: argument
-// validation on the host, then one kernel launch on the caller's stream.
+// validation on the host, then kernel launches on the caller's stream.
+//
+// Kernels: the pipelined streaming kernels (kernels_stream.cu) serve every
+// call.  Setting MASKLLM_KERNELS=direct in the environment selects the
+// per-matrix kernels with direct vector loads instead (kernels_mask.cu,
+// kernels_pack.cu); both compute the same results and exist side by side so
+// their throughput can be compared on the same build.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
@@ -26,6 +33,14 @@ maskllm_status cuda_fail(cudaError_t e) {
   return MASKLLM_ERR_CUDA;
 }
 
+bool use_direct_kernels() {
+  static const bool direct = [] {
+    const char* v = getenv("MASKLLM_KERNELS");
+    return v != nullptr && strcmp(v, "direct") == 0;
+  }();
+  return direct;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Span {
@@ -39,16 +54,24 @@ bool overlaps(Span a, Span b) {
   return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
 }
 
-// Outputs must not overlap inputs nor each other.
-maskllm_status check_alias(const Span* in, int n_in, const Span* out, int n_out) {
-  for (int o = 0; o < n_out; ++o) {
-    for (int i = 0; i < n_in; ++i)
-      if (overlaps(out[o], in[i])) return MASKLLM_ERR_ALIAS;
-    for (int o2 = o + 1; o2 < n_out; ++o2)
-      if (overlaps(out[o], out[o2])) return MASKLLM_ERR_ALIAS;
+// Inputs and outputs of one call (all matrices of a batch together).
+struct Spans {
+  Span in[3 * kMaxBatch];
+  Span out[3 * kMaxBatch];
+  int n_in = 0, n_out = 0;
+  void input(const void* p, uint64_t b) { in[n_in++] = {p, b}; }
+  void output(const void* p, uint64_t b) { out[n_out++] = {p, b}; }
+  // Outputs must not overlap inputs nor each other.
+  maskllm_status check() const {
+    for (int o = 0; o < n_out; ++o) {
+      for (int i = 0; i < n_in; ++i)
+        if (overlaps(out[o], in[i])) return MASKLLM_ERR_ALIAS;
+      for (int o2 = o + 1; o2 < n_out; ++o2)
+        if (overlaps(out[o], out[o2])) return MASKLLM_ERR_ALIAS;
+    }
+    return MASKLLM_OK;
   }
-  return MASKLLM_OK;
-}
+};
 
 maskllm_status check_shape(int64_t rows, int64_t cols) {
   if (rows < 1 || cols < 32 || cols % 32 != 0) return MASKLLM_ERR_SHAPE;
@@ -75,18 +98,195 @@ maskllm_status check_temperature(float tau, float kappa) {
   return MASKLLM_OK;
 }
 
-#define MK_TRY(expr)                      \
-  do {                                    \
-    const maskllm_status st_ = (expr);    \
-    if (st_ != MASKLLM_OK) return st_;    \
+#define MK_TRY(expr)                   \
+  do {                                 \
+    const maskllm_status st_ = (expr); \
+    if (st_ != MASKLLM_OK) return st_; \
   } while (0)
 
-maskllm_status get_device(Device* d) {
-  const cudaError_t e = current_device(d);
-  return e == cudaSuccess ? MASKLLM_OK : cuda_fail(e);
+uint64_t weights(const maskllm_matrix& m) {
+  return static_cast<uint64_t>(m.rows) * static_cast<uint64_t>(m.cols);
+}
+
+// Per-operation validation of one matrix; appends its spans.
+maskllm_status check_prior(const maskllm_matrix& m, Spans& sp) {
+  const void* ptrs[] = {m.W, m.logits_out};
+  MK_TRY(check_ptrs(ptrs, 2));
+  MK_TRY(check_shape(m.rows, m.cols));
+  const uint64_t n = weights(m);
+  sp.input(m.W, 2 * n);
+  sp.output(m.logits_out, 6 * n);
+  return MASKLLM_OK;
+}
+
+maskllm_status check_forward(const maskllm_matrix& m, Spans& sp) {
+  const void* ptrs[] = {m.W, m.logits, m.W_out};
+  MK_TRY(check_ptrs(ptrs, 3));
+  MK_TRY(check_optional(m.row_sq_out));
+  MK_TRY(check_optional(m.probs_out));
+  MK_TRY(check_shape(m.rows, m.cols));
+  const uint64_t n = weights(m);
+  sp.input(m.W, 2 * n);
+  sp.input(m.logits, 6 * n);
+  sp.output(m.W_out, 2 * n);
+  sp.output(m.row_sq_out, 4 * static_cast<uint64_t>(m.rows));
+  sp.output(m.probs_out, 6 * n);
+  return MASKLLM_OK;
+}
+
+maskllm_status check_backward(const maskllm_matrix& m, Spans& sp) {
+  const void* ptrs[] = {m.W, m.logits, m.grad_W_out, m.dlogits_out};
+  MK_TRY(check_ptrs(ptrs, 4));
+  MK_TRY(check_shape(m.rows, m.cols));
+  const uint64_t n = weights(m);
+  sp.input(m.W, 2 * n);
+  sp.input(m.logits, 6 * n);
+  sp.input(m.grad_W_out, 2 * n);
+  sp.output(m.dlogits_out, 6 * n);
+  return MASKLLM_OK;
+}
+
+maskllm_status check_compress(const maskllm_matrix& m, Spans& sp) {
+  const void* ptrs[] = {m.W, m.logits, m.values_out, m.meta_out};
+  MK_TRY(check_ptrs(ptrs, 4));
+  MK_TRY(check_optional(m.idx_out));
+  MK_TRY(check_shape(m.rows, m.cols));
+  const uint64_t n = weights(m);
+  sp.input(m.W, 2 * n);
+  sp.input(m.logits, 6 * n);
+  sp.output(m.values_out, n);
+  sp.output(m.meta_out, n / 8);
+  sp.output(m.idx_out, n / 4);
+  return MASKLLM_OK;
 }
 
 maskllm_status finish(cudaError_t e) { return e == cudaSuccess ? MASKLLM_OK : cuda_fail(e); }
+
+enum class Op { kPrior, kForward, kBackward, kCompress };
+
+struct Call {
+  Op op;
+  float tau = 1.0f, kappa = 0.0f, reg = 0.0f, scale = 1.0f;
+  uint64_t seed = 0;
+  uint32_t step = 0;
+};
+
+StreamMatrix to_stream(const maskllm_matrix& m, Op op) {
+  StreamMatrix s{};
+  s.W = m.W;
+  s.L = m.logits;
+  s.G = m.grad_W_out;
+  s.rows = m.rows;
+  s.cols = m.cols;
+  s.tensor_id = m.tensor_id;
+  switch (op) {
+    case Op::kPrior: s.out0 = m.logits_out; break;
+    case Op::kForward:
+      s.out0 = m.W_out;
+      s.out1 = m.row_sq_out;
+      s.out2 = m.probs_out;
+      break;
+    case Op::kBackward: s.out0 = m.dlogits_out; break;
+    case Op::kCompress:
+      s.out0 = m.values_out;
+      s.out1 = m.meta_out;
+      s.out2 = m.idx_out;
+      break;
+  }
+  return s;
+}
+
+cudaError_t run_direct(const Device& d, const Call& c, const maskllm_matrix& m, cudaStream_t s) {
+  const RngArgs rng{c.seed, c.step, m.tensor_id};
+  switch (c.op) {
+    case Op::kPrior: return launch_prior_init(d, m.W, m.rows, m.cols, c.scale, m.logits_out, s);
+    case Op::kForward:
+      return launch_forward(d, m.W, m.logits, m.rows, m.cols, c.tau, c.kappa, rng, m.W_out,
+                            m.row_sq_out, m.probs_out, s);
+    case Op::kBackward:
+      return launch_backward(d, m.W, m.logits, m.grad_W_out, m.rows, m.cols, c.tau, c.kappa, rng,
+                             c.reg, m.dlogits_out, s);
+    case Op::kCompress:
+      return launch_hard_compress(d, m.W, m.logits, m.rows, m.cols, m.values_out, m.meta_out,
+                                  m.idx_out, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+maskllm_status run(const Call& c, const maskllm_matrix* mats, int32_t n, cudaStream_t s) {
+  if (mats == nullptr || n < 1) return MASKLLM_ERR_INVALID_ARG;
+  if (c.op == Op::kForward || c.op == Op::kBackward) MK_TRY(check_temperature(c.tau, c.kappa));
+  if (!isfinite(c.reg) || !isfinite(c.scale)) return MASKLLM_ERR_INVALID_ARG;
+  // validate everything before launching anything
+  for (int32_t b = 0; b < n; b += kMaxBatch) {
+    const int32_t nb = n - b < kMaxBatch ? n - b : kMaxBatch;
+    Spans sp;
+    for (int32_t i = 0; i < nb; ++i) {
+      const maskllm_matrix& m = mats[b + i];
+      switch (c.op) {
+        case Op::kPrior: MK_TRY(check_prior(m, sp)); break;
+        case Op::kForward: MK_TRY(check_forward(m, sp)); break;
+        case Op::kBackward: MK_TRY(check_backward(m, sp)); break;
+        case Op::kCompress: MK_TRY(check_compress(m, sp)); break;
+      }
+    }
+    MK_TRY(sp.check());
+  }
+  if (n > kMaxBatch) {
+    // outputs of one launch must not overlap inputs or outputs of another
+    for (int32_t i = 0; i < n; ++i) {
+      Spans one;
+      switch (c.op) {
+        case Op::kPrior: check_prior(mats[i], one); break;
+        case Op::kForward: check_forward(mats[i], one); break;
+        case Op::kBackward: check_backward(mats[i], one); break;
+        case Op::kCompress: check_compress(mats[i], one); break;
+      }
+      for (int32_t j = 0; j < n; ++j) {
+        if (j == i) continue;
+        Spans other;
+        switch (c.op) {
+          case Op::kPrior: check_prior(mats[j], other); break;
+          case Op::kForward: check_forward(mats[j], other); break;
+          case Op::kBackward: check_backward(mats[j], other); break;
+          case Op::kCompress: check_compress(mats[j], other); break;
+        }
+        for (int o = 0; o < one.n_out; ++o) {
+          for (int k = 0; k < other.n_in; ++k)
+            if (overlaps(one.out[o], other.in[k])) return MASKLLM_ERR_ALIAS;
+          for (int k = 0; k < other.n_out; ++k)
+            if (overlaps(one.out[o], other.out[k])) return MASKLLM_ERR_ALIAS;
+        }
+      }
+    }
+  }
+  Device d;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (use_direct_kernels()) {
+    for (int32_t i = 0; i < n; ++i)
+      if ((e = run_direct(d, c, mats[i], s)) != cudaSuccess) return cuda_fail(e);
+    return MASKLLM_OK;
+  }
+  for (int32_t b = 0; b < n; b += kMaxBatch) {
+    const int32_t nb = n - b < kMaxBatch ? n - b : kMaxBatch;
+    StreamMatrix sm[kMaxBatch];
+    bool probs = false;
+    for (int32_t i = 0; i < nb; ++i) {
+      sm[i] = to_stream(mats[b + i], c.op);
+      probs = probs || (c.op == Op::kForward && mats[b + i].probs_out != nullptr);
+    }
+    const RngArgs rng{c.seed, c.step, 0};
+    switch (c.op) {
+      case Op::kPrior: e = stream_prior_init(d, sm, nb, c.scale, s); break;
+      case Op::kForward: e = stream_forward(d, sm, nb, c.tau, c.kappa, rng, probs, s); break;
+      case Op::kBackward: e = stream_backward(d, sm, nb, c.tau, c.kappa, rng, c.reg, s); break;
+      case Op::kCompress: e = stream_hard_compress(d, sm, nb, s); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return MASKLLM_OK;
+}
 
 }  // namespace
 
@@ -107,84 +307,112 @@ cudaError_t current_device(Device* d) {
 
 }  // namespace maskllm
 
-using maskllm::Span;
+using maskllm::Call;
+using maskllm::Op;
 
 extern "C" {
 
 maskllm_status maskllm_prior_init(const uint16_t* W, int64_t rows, int64_t cols, float scale,
                                   float* logits_out, maskllm_stream_t stream) {
-  const void* ptrs[] = {W, logits_out};
-  MK_TRY(maskllm::check_ptrs(ptrs, 2));
-  MK_TRY(maskllm::check_shape(rows, cols));
-  if (!isfinite(scale)) return MASKLLM_ERR_INVALID_ARG;
-  const uint64_t n = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols);
-  const Span in[] = {{W, 2 * n}};
-  const Span out[] = {{logits_out, 6 * n}};
-  MK_TRY(maskllm::check_alias(in, 1, out, 1));
-  maskllm::Device d;
-  MK_TRY(maskllm::get_device(&d));
-  return maskllm::finish(
-      maskllm::launch_prior_init(d, W, rows, cols, scale, logits_out, stream));
+  maskllm_matrix m{};
+  m.W = W;
+  m.rows = rows;
+  m.cols = cols;
+  m.logits_out = logits_out;
+  Call c{Op::kPrior};
+  c.scale = scale;
+  return maskllm::run(c, &m, 1, stream);
 }
 
 maskllm_status maskllm_forward(const uint16_t* W, const float* logits, int64_t rows,
                                int64_t cols, float tau, float kappa, maskllm_rng rng,
                                uint16_t* W_out, float* row_sq_out, float* probs_out,
                                maskllm_stream_t stream) {
-  const void* ptrs[] = {W, logits, W_out};
-  MK_TRY(maskllm::check_ptrs(ptrs, 3));
-  MK_TRY(maskllm::check_optional(row_sq_out));
-  MK_TRY(maskllm::check_optional(probs_out));
-  MK_TRY(maskllm::check_shape(rows, cols));
-  MK_TRY(maskllm::check_temperature(tau, kappa));
-  const uint64_t n = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols);
-  const Span in[] = {{W, 2 * n}, {logits, 6 * n}};
-  const Span out[] = {{W_out, 2 * n},
-                      {row_sq_out, 4 * static_cast<uint64_t>(rows)},
-                      {probs_out, 6 * n}};
-  MK_TRY(maskllm::check_alias(in, 2, out, 3));
-  maskllm::Device d;
-  MK_TRY(maskllm::get_device(&d));
-  return maskllm::finish(maskllm::launch_forward(d, W, logits, rows, cols, tau, kappa,
-                                                 {rng.seed, rng.step, rng.tensor_id}, W_out,
-                                                 row_sq_out, probs_out, stream));
+  maskllm_matrix m{};
+  m.W = W;
+  m.logits = logits;
+  m.rows = rows;
+  m.cols = cols;
+  m.tensor_id = rng.tensor_id;
+  m.W_out = W_out;
+  m.row_sq_out = row_sq_out;
+  m.probs_out = probs_out;
+  Call c{Op::kForward};
+  c.tau = tau;
+  c.kappa = kappa;
+  c.seed = rng.seed;
+  c.step = rng.step;
+  return maskllm::run(c, &m, 1, stream);
 }
 
 maskllm_status maskllm_backward(const uint16_t* W, const float* logits,
                                 const uint16_t* grad_W_out, int64_t rows, int64_t cols,
                                 float tau, float kappa, maskllm_rng rng, float reg_coeff,
                                 float* dlogits_out, maskllm_stream_t stream) {
-  const void* ptrs[] = {W, logits, grad_W_out, dlogits_out};
-  MK_TRY(maskllm::check_ptrs(ptrs, 4));
-  MK_TRY(maskllm::check_shape(rows, cols));
-  MK_TRY(maskllm::check_temperature(tau, kappa));
-  if (!isfinite(reg_coeff)) return MASKLLM_ERR_INVALID_ARG;
-  const uint64_t n = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols);
-  const Span in[] = {{W, 2 * n}, {logits, 6 * n}, {grad_W_out, 2 * n}};
-  const Span out[] = {{dlogits_out, 6 * n}};
-  MK_TRY(maskllm::check_alias(in, 3, out, 1));
-  maskllm::Device d;
-  MK_TRY(maskllm::get_device(&d));
-  return maskllm::finish(maskllm::launch_backward(d, W, logits, grad_W_out, rows, cols, tau,
-                                                  kappa, {rng.seed, rng.step, rng.tensor_id},
-                                                  reg_coeff, dlogits_out, stream));
+  maskllm_matrix m{};
+  m.W = W;
+  m.logits = logits;
+  m.grad_W_out = grad_W_out;
+  m.rows = rows;
+  m.cols = cols;
+  m.tensor_id = rng.tensor_id;
+  m.dlogits_out = dlogits_out;
+  Call c{Op::kBackward};
+  c.tau = tau;
+  c.kappa = kappa;
+  c.seed = rng.seed;
+  c.step = rng.step;
+  c.reg = reg_coeff;
+  return maskllm::run(c, &m, 1, stream);
 }
 
 maskllm_status maskllm_hard_compress(const uint16_t* W, const float* logits, int64_t rows,
                                      int64_t cols, uint16_t* values_out, uint32_t* meta_out,
                                      uint8_t* idx_out, maskllm_stream_t stream) {
-  const void* ptrs[] = {W, logits, values_out, meta_out};
-  MK_TRY(maskllm::check_ptrs(ptrs, 4));
-  MK_TRY(maskllm::check_optional(idx_out));
-  MK_TRY(maskllm::check_shape(rows, cols));
-  const uint64_t n = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols);
-  const Span in[] = {{W, 2 * n}, {logits, 6 * n}};
-  const Span out[] = {{values_out, n}, {meta_out, n / 8}, {idx_out, n / 4}};
-  MK_TRY(maskllm::check_alias(in, 2, out, 3));
-  maskllm::Device d;
-  MK_TRY(maskllm::get_device(&d));
-  return maskllm::finish(maskllm::launch_hard_compress(d, W, logits, rows, cols, values_out,
-                                                       meta_out, idx_out, stream));
+  maskllm_matrix m{};
+  m.W = W;
+  m.logits = logits;
+  m.rows = rows;
+  m.cols = cols;
+  m.values_out = values_out;
+  m.meta_out = meta_out;
+  m.idx_out = idx_out;
+  return maskllm::run(Call{Op::kCompress}, &m, 1, stream);
+}
+
+maskllm_status maskllm_prior_init_batched(const maskllm_matrix* mats, int32_t n, float scale,
+                                          maskllm_stream_t stream) {
+  Call c{Op::kPrior};
+  c.scale = scale;
+  return maskllm::run(c, mats, n, stream);
+}
+
+maskllm_status maskllm_forward_batched(const maskllm_matrix* mats, int32_t n, float tau,
+                                       float kappa, uint64_t seed, uint32_t step,
+                                       maskllm_stream_t stream) {
+  Call c{Op::kForward};
+  c.tau = tau;
+  c.kappa = kappa;
+  c.seed = seed;
+  c.step = step;
+  return maskllm::run(c, mats, n, stream);
+}
+
+maskllm_status maskllm_backward_batched(const maskllm_matrix* mats, int32_t n, float tau,
+                                        float kappa, uint64_t seed, uint32_t step,
+                                        float reg_coeff, maskllm_stream_t stream) {
+  Call c{Op::kBackward};
+  c.tau = tau;
+  c.kappa = kappa;
+  c.seed = seed;
+  c.step = step;
+  c.reg = reg_coeff;
+  return maskllm::run(c, mats, n, stream);
+}
+
+maskllm_status maskllm_hard_compress_batched(const maskllm_matrix* mats, int32_t n,
+                                             maskllm_stream_t stream) {
+  return maskllm::run(Call{Op::kCompress}, mats, n, stream);
 }
 
 maskllm_status maskllm_decompress(const uint16_t* values, const uint32_t* meta, int64_t rows,
@@ -193,11 +421,14 @@ maskllm_status maskllm_decompress(const uint16_t* values, const uint32_t* meta, 
   MK_TRY(maskllm::check_ptrs(ptrs, 3));
   MK_TRY(maskllm::check_shape(rows, cols));
   const uint64_t n = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols);
-  const Span in[] = {{values, n}, {meta, n / 8}};
-  const Span out[] = {{W_out, 2 * n}};
-  MK_TRY(maskllm::check_alias(in, 2, out, 1));
+  maskllm::Spans sp;
+  sp.input(values, n);
+  sp.input(meta, n / 8);
+  sp.output(W_out, 2 * n);
+  MK_TRY(sp.check());
   maskllm::Device d;
-  MK_TRY(maskllm::get_device(&d));
+  cudaError_t e = maskllm::current_device(&d);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
   return maskllm::finish(maskllm::launch_decompress(d, values, meta, rows, cols, W_out, stream));
 }
 
@@ -209,16 +440,28 @@ maskllm_status maskllm_noise_words(maskllm_rng rng, int64_t group_begin, int64_t
       group_begin > (int64_t(1) << 62) - n)
     return MASKLLM_ERR_INVALID_ARG;
   maskllm::Device d;
-  MK_TRY(maskllm::get_device(&d));
+  cudaError_t e = maskllm::current_device(&d);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
   return maskllm::finish(maskllm::launch_noise_words(
       d, {rng.seed, rng.step, rng.tensor_id}, group_begin, n, out4, stream));
 }
 
+maskllm_status maskllm_set_wait_timeout(uint64_t nanoseconds) {
+  maskllm::stream_set_wait_ns(nanoseconds);
+  return MASKLLM_OK;
+}
+
+maskllm_status maskllm_test_withhold_loads(int32_t enable) {
+  maskllm::stream_set_withhold_loads(enable != 0);
+  return MASKLLM_OK;
+}
+
 maskllm_status maskllm_device_status(maskllm_stream_t stream) {
-  uint32_t word = 0;
-  const cudaError_t e = maskllm::read_and_clear_error_word(stream, &word);
+  uint32_t a = 0, b = 0;
+  cudaError_t e = maskllm::read_and_clear_error_word(stream, &a);
+  if (e == cudaSuccess) e = maskllm::read_and_clear_stream_error(stream, &b);
   if (e != cudaSuccess) return maskllm::cuda_fail(e);
-  return word != 0 ? MASKLLM_ERR_TIMEOUT : MASKLLM_OK;
+  return (a | b) != 0 ? MASKLLM_ERR_TIMEOUT : MASKLLM_OK;
 }
 
 const char* maskllm_status_string(maskllm_status status) {

@@ -107,3 +107,42 @@ def test_binding_refuses_host_tensors(L):
     W = torch.zeros((4, 64), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         binding.maskllm_prior_init(W, 1.0)
+
+
+def _mat(**kw):
+    from semi_structured_sparsity_gb300 import binding
+    m = binding.maskllm_matrix()
+    m.rows, m.cols = kw.pop("rows", 4), kw.pop("cols", 64)
+    for k, v in kw.items():
+        setattr(m, k, v)
+    return m
+
+
+def test_batched_validation(L):
+    from semi_structured_sparsity_gb300 import binding
+    arr = (binding.maskllm_matrix * 3)()
+    assert L.maskllm_forward_batched(arr, 0, 1.0, 1.0, 0, 0, None) == INVALID
+    assert L.maskllm_forward_batched(None, 1, 1.0, 1.0, 0, 0, None) == INVALID
+    # matrix 1 is missing its output
+    arr[0] = _mat(W=A, logits=B, W_out=Cc)
+    arr[1] = _mat(W=D, logits=E)
+    assert L.maskllm_forward_batched(arr, 2, 1.0, 1.0, 0, 0, None) == INVALID
+    # matrix 1 writes over matrix 0's logits
+    arr[1] = _mat(W=D, logits=E, W_out=B + 64)
+    assert L.maskllm_forward_batched(arr, 2, 1.0, 1.0, 0, 0, None) == ALIAS
+    arr[1] = _mat(W=D, logits=E, W_out=0x600000, rows=4, cols=40)
+    assert L.maskllm_forward_batched(arr, 2, 1.0, 1.0, 0, 0, None) == SHAPE
+    assert L.maskllm_backward_batched(arr, 1, 1.0, 1.0, 0, 0, 0.0, None) == INVALID
+    assert L.maskllm_forward_batched(arr, 1, -1.0, 1.0, 0, 0, None) == INVALID
+
+
+def test_batched_alias_across_launches(L):
+    from semi_structured_sparsity_gb300 import binding
+    n = 20   # more than one launch's worth
+    arr = (binding.maskllm_matrix * n)()
+    base = 0x10000000
+    for i in range(n):
+        off = base + i * 0x100000
+        arr[i] = _mat(W=off, logits_out=off + 0x10000)
+    arr[19].logits_out = base + 0x10        # writes over matrix 0's W, in another launch
+    assert L.maskllm_prior_init_batched(arr, n, 1.0, None) == ALIAS

@@ -1,0 +1,180 @@
+"""GPU: batched calls (several matrices per launch) against the oracle and the
+single-matrix calls; the per-matrix direct-load kernels (selected with
+MASKLLM_KERNELS=direct) against the oracle; and the bounded-wait timeout path
+(a wait that runs out sets the device error word, the context stays usable)."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from semi_structured_sparsity_gb300 import binding as mk
+from semi_structured_sparsity_gb300 import workloads as wl
+from tests._helpers import (assert_bf16_ulps, assert_bits_equal, assert_close, bits16, bits32,
+                            ROWSQ_RTOL)
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# mixed shapes: long rows with ragged chunks, rows of exactly one chunk, short
+# rows packed several per chunk, odd row counts
+BATCH = [(37, 4128), (16, 4096), (5, 11008), (300, 64), (9, 1056), (64, 224), (3, 96)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mk.lib()
+
+
+def _mats(shapes, seed=0):
+    out = []
+    for i, (r, c) in enumerate(shapes):
+        W, L, G = wl.random_case(r, c, seed=seed + i, device="cuda")
+        out.append({"W": W, "logits": L, "grad_W_out": G, "tensor_id": 100 + i,
+                    "logits_out": torch.empty_like(L),
+                    "W_out": torch.empty_like(W),
+                    "row_sq_out": torch.empty((r,), device="cuda"),
+                    "probs_out": torch.empty_like(L),
+                    "dlogits_out": torch.empty_like(L),
+                    "values_out": torch.empty((r, c // 2), dtype=torch.bfloat16, device="cuda"),
+                    "meta_out": torch.empty((r, c // 32), dtype=torch.int32, device="cuda"),
+                    "idx_out": torch.empty((r, c // 4), dtype=torch.uint8, device="cuda")})
+    return out
+
+
+@pytest.mark.parametrize("n", [len(BATCH), 20])
+def test_batched_calls_match_oracle(n):
+    shapes = (BATCH * 3)[:n]
+    mats = _mats(shapes, seed=3)
+    tau, kappa, seed, step, reg = 2.0, 50.0, 77, 5, 0.1
+    mk.maskllm_prior_init_batched(mats, 300.0)
+    mk.maskllm_forward_batched(mats, tau, kappa, seed, step)
+    mk.maskllm_backward_batched(mats, tau, kappa, seed, step, reg_coeff=reg)
+    mk.maskllm_hard_compress_batched(mats)
+    torch.cuda.synchronize()
+    assert mk.maskllm_device_status() == 0
+    for m in mats:
+        Wb, Lh, Gb = bits16(m["W"]), m["logits"].cpu().numpy(), bits16(m["grad_W_out"])
+        rows, cols = m["W"].shape
+        tid = m["tensor_id"]
+        assert_bits_equal(bits32(m["logits_out"]), orc.prior_init(Wb, 300.0).view(np.uint32),
+                          "prior")
+        wW, wsq, wp, _ = orc.forward(Wb, Lh, tau, kappa, seed, step, tid, want_probs=True)
+        assert_bf16_ulps(bits16(m["W_out"]), wW)
+        assert_close(m["probs_out"].cpu().numpy(), wp, what="p")
+        assert_close(m["row_sq_out"].cpu().numpy(), wsq, rtol=ROWSQ_RTOL, atol=0, what="row_sq")
+        assert_close(m["dlogits_out"].cpu().numpy(),
+                     orc.backward(Wb, Lh, Gb, tau, kappa, seed, step, tid, reg), what="dlogits")
+        wv, wm, wi = orc.hard_compress(Wb, Lh)
+        assert_bits_equal(bits16(m["values_out"]), wv, "values")
+        assert_bits_equal(bits32(m["meta_out"]), wm, "meta")
+        assert_bits_equal(m["idx_out"].cpu().numpy(), wi, "idx")
+
+
+def test_batched_equals_single_calls_bitwise():
+    mats = _mats(BATCH, seed=11)
+    tau, kappa, seed, step = 1.0, 300.0, 1, 2
+    mk.maskllm_forward_batched(mats, tau, kappa, seed, step)
+    mk.maskllm_backward_batched(mats, tau, kappa, seed, step)
+    for m in mats:
+        Wo, sq, _ = mk.maskllm_forward(m["W"], m["logits"], tau, kappa,
+                                       (seed, step, m["tensor_id"]))
+        dL = mk.maskllm_backward(m["W"], m["logits"], m["grad_W_out"], tau, kappa,
+                                 (seed, step, m["tensor_id"]))
+        torch.cuda.synchronize()
+        assert_bits_equal(bits16(Wo), bits16(m["W_out"]), "W' batched vs single")
+        assert_bits_equal(bits32(sq), bits32(m["row_sq_out"]), "row_sq batched vs single")
+        assert_bits_equal(bits32(dL), bits32(m["dlogits_out"]), "dlogits batched vs single")
+
+
+def test_batched_optional_outputs_may_be_null_per_matrix():
+    mats = _mats(BATCH[:3], seed=21)
+    mats[1]["probs_out"] = None
+    mats[2]["row_sq_out"] = None
+    mats[0]["idx_out"] = None
+    mk.maskllm_forward_batched(mats, 4.0, 100.0, 0, 0)
+    mk.maskllm_hard_compress_batched(mats)
+    torch.cuda.synchronize()
+    for m in mats:
+        Wb, Lh = bits16(m["W"]), m["logits"].cpu().numpy()
+        wW, wsq, wp, _ = orc.forward(Wb, Lh, 4.0, 100.0, 0, 0, m["tensor_id"], want_probs=True)
+        assert_bf16_ulps(bits16(m["W_out"]), wW)
+        if m["row_sq_out"] is not None:
+            assert_close(m["row_sq_out"].cpu().numpy(), wsq, rtol=ROWSQ_RTOL, atol=0)
+        wv, wm, _ = orc.hard_compress(Wb, Lh)
+        assert_bits_equal(bits32(m["meta_out"]), wm, "meta")
+
+
+def test_batched_rejects_cross_matrix_alias():
+    mats = _mats(BATCH[:2], seed=31)
+    mats[1]["dlogits_out"] = mats[0]["logits"]          # an output over another matrix's input
+    with pytest.raises(mk.MaskLLMError) as e:
+        mk.maskllm_backward_batched(mats, 1.0, 1.0, 0, 0)
+    assert e.value.status == 4
+
+
+_DIRECT_SCRIPT = r"""
+import json, sys, torch
+sys.path.insert(0, {root!r})
+from semi_structured_sparsity_gb300 import binding as mk, workloads as wl
+out = {{}}
+for i, (r, c) in enumerate({shapes!r}):
+    W, L, G = wl.random_case(r, c, seed=40 + i, device="cuda")
+    Wo, sq, _ = mk.maskllm_forward(W, L, 4.0, 100.0, (0, 0, 0))
+    dL = mk.maskllm_backward(W, L, G, 4.0, 100.0, (0, 0, 0), reg_coeff=0.25)
+    v, m, _ = mk.maskllm_hard_compress(W, L)
+    P = mk.maskllm_prior_init(W, 300.0)
+    torch.cuda.synchronize()
+    torch.save({{"Wo": Wo.cpu(), "sq": sq.cpu(), "dL": dL.cpu(), "v": v.cpu(), "m": m.cpu(),
+                "P": P.cpu()}}, {tmp!r} + "/out%d.pt" % i)
+"""
+
+
+def test_direct_kernels_match_oracle(tmp_path):
+    shapes = [(7, 160), (33, 11008), (256, 1024), (300, 64)]
+    script = _DIRECT_SCRIPT.format(root=ROOT, shapes=shapes, tmp=str(tmp_path))
+    env = dict(os.environ, MASKLLM_KERNELS="direct")
+    r = subprocess.run([sys.executable, "-c", script], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    for i, (rows, cols) in enumerate(shapes):
+        got = torch.load(str(tmp_path / ("out%d.pt" % i)))
+        W, L, G = wl.random_case(rows, cols, seed=40 + i, device="cuda")
+        Wb, Lh, Gb = bits16(W), L.cpu().numpy(), bits16(G)
+        wW, wsq, _, _ = orc.forward(Wb, Lh, 4.0, 100.0, 0)
+        assert_bf16_ulps(bits16(got["Wo"]), wW)
+        assert_close(got["sq"].numpy(), wsq, rtol=ROWSQ_RTOL, atol=0, what="row_sq")
+        assert_close(got["dL"].numpy(), orc.backward(Wb, Lh, Gb, 4.0, 100.0, 0, reg_coeff=0.25),
+                     what="dlogits")
+        wv, wm, _ = orc.hard_compress(Wb, Lh)
+        assert_bits_equal(bits16(got["v"]), wv, "values")
+        assert_bits_equal(bits32(got["m"]), wm, "meta")
+        assert_bits_equal(bits32(got["P"]), orc.prior_init(Wb, 300.0).view(np.uint32), "prior")
+
+
+def test_wait_timeout_sets_error_and_context_survives():
+    """A wait that nothing will satisfy (the producer is told to issue no copies)
+    gives up after the configured bound; the kernel returns, the error word
+    reads MASKLLM_ERR_TIMEOUT, and the next launches work normally."""
+    W, L, G = wl.random_case(8, 1024, seed=50, device="cuda")
+    assert mk.maskllm_device_status() == 0
+    try:
+        mk.maskllm_set_wait_timeout(50_000_000)       # 50 ms
+        mk.maskllm_test_withhold_loads(True)
+        mk.maskllm_forward(W, L, 1.0, 10.0, (0, 0, 0))
+        mk.maskllm_backward(W, L, G, 1.0, 10.0, (0, 0, 0))
+        assert mk.maskllm_device_status() == 6      # MASKLLM_ERR_TIMEOUT
+        assert mk.maskllm_device_status() == 0      # read clears it
+    finally:
+        mk.maskllm_test_withhold_loads(False)
+        mk.maskllm_set_wait_timeout(2_000_000_000)
+    Wo, sq, _ = mk.maskllm_forward(W, L, 1.0, 10.0, (0, 0, 0))
+    torch.cuda.synchronize()
+    assert mk.maskllm_device_status() == 0
+    assert_bf16_ulps(bits16(Wo), orc.forward(bits16(W), L.cpu().numpy(), 1.0, 10.0, 0)[0])
