@@ -70,23 +70,26 @@ __device__ __forceinline__ uint4 group_words(uint64_t gidx, uint32_t step, uint3
 
 // Gumbel noise of the six candidates: candidate c reads the 16-bit half
 // (c & 1) of word (c >> 1), low half first, and its top 14 bits index the
-// quantile table (resident in shared memory).
-__device__ __forceinline__ void gumbel6(const uint4 w, const float* __restrict__ tab,
-                                        float g[kCand]) {
-  g[0] = tab[(w.x >> 2) & 0x3FFFu];
-  g[1] = tab[w.x >> 18];
-  g[2] = tab[(w.y >> 2) & 0x3FFFu];
-  g[3] = tab[w.y >> 18];
-  g[4] = tab[(w.z >> 2) & 0x3FFFu];
-  g[5] = tab[w.z >> 18];
+// quantile table (resident in shared memory).  The byte offset of cell
+// (h >> 2) is h & ~3, taken straight from the word.
+__device__ __forceinline__ float table_at(const float* tab, uint32_t byte_offset) {
+  return *reinterpret_cast<const float*>(reinterpret_cast<const char*>(tab) + byte_offset);
 }
 
-// 2^x without flushing subnormal results to zero: candidates whose
-// probability falls below 2^-126 still contribute to the soft mask, so W'
-// keeps its bf16 subnormals.
+__device__ __forceinline__ void gumbel6(const uint4 w, const float* __restrict__ tab,
+                                        float g[kCand]) {
+  g[0] = table_at(tab, w.x & 0xFFFCu);
+  g[1] = table_at(tab, (w.x >> 16) & 0xFFFCu);
+  g[2] = table_at(tab, w.y & 0xFFFCu);
+  g[3] = table_at(tab, (w.y >> 16) & 0xFFFCu);
+  g[4] = table_at(tab, w.z & 0xFFFCu);
+  g[5] = table_at(tab, (w.z >> 16) & 0xFFFCu);
+}
+
+// 2^x, flushing subnormal results to zero (one MUFU operation).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -96,33 +99,46 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
+// Exponent offset of the unnormalised softmax terms: e_c = 2^(d_c + 64) with
+// d_c = (z_c - max z) log2 e <= ~0, so the largest term is ~2^64 and terms
+// down to 2^-190 of it stay normal fp32 numbers when ex2 flushes subnormals.
+// Anything smaller cannot reach a bf16 W' (w * M < 2^-190 rounds to zero;
+// the smallest bf16 subnormal is 2^-133).  The factor cancels in e_c / sum e.
+constexpr float kExpOffset = 64.0f;
+
 // Unnormalised softmax of one group.  The noisy logit
 //   z_c = fl(fl(fl(kappa * L_c) + g_c) * rho)
 // is formed with explicitly rounded operations (no contraction), so it is
 // bit-identical to any other IEEE implementation of the same three steps.
-// Then e_c = 2^(z_c log2 e - m log2 e) with m = max z: the shift is common to
-// all six terms and cancels in p_c = e_c / sum e.
+// Then e_c = 2^(z_c log2 e - m log2 e + 64) with m = max z: the shift is
+// common to all six terms and cancels in p_c = e_c / sum e.  Also returns the
+// four soft-mask numerators n_j = sum of e_c over the candidates keeping j:
+// position 0: c0 (0,1) c1 (0,2) c2 (0,3);  position 1: c0, c3 (1,2), c4 (1,3);
+// position 2: c1, c3, c5 (2,3);            position 3: c2, c4, c5.
 __device__ __forceinline__ void softmax6(const float L[kCand], const float g[kCand], float kappa,
-                                         float rho, float e[kCand], float& inv_sum) {
+                                         float rho, float e[kCand], float& inv_sum,
+                                         float num[4]) {
   float z[kCand];
 #pragma unroll
   for (int c = 0; c < kCand; ++c) z[c] = __fmul_rn(__fadd_rn(__fmul_rn(kappa, L[c]), g[c]), rho);
   const float m = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])), fmaxf(z[4], z[5]));
-  const float ml = __fmul_rn(m, kLog2e);
+  const float shift = kExpOffset - __fmul_rn(m, kLog2e);
 #pragma unroll
-  for (int c = 0; c < kCand; ++c) e[c] = ex2_approx(__fmaf_rn(z[c], kLog2e, -ml));
-  const float s = (e[0] + e[1]) + (e[2] + e[3]) + (e[4] + e[5]);
-  inv_sum = rcp_approx(s);
+  for (int c = 0; c < kCand; ++c) e[c] = ex2_approx(__fmaf_rn(z[c], kLog2e, shift));
+  const float e34 = e[3] + e[4];
+  const float e35 = e[3] + e[5];
+  const float e45 = e[4] + e[5];
+  num[0] = (e[0] + e[1]) + e[2];
+  num[1] = e[0] + e34;
+  num[2] = e[1] + e35;
+  num[3] = e[2] + e45;
+  inv_sum = rcp_approx(num[0] + e34 + e[5]);
 }
 
-// Soft mask M_j = sum of p_c over the candidates keeping position j:
-// position 0: c0 (0,1) c1 (0,2) c2 (0,3);  position 1: c0, c3 (1,2), c4 (1,3);
-// position 2: c1, c3, c5 (2,3);            position 3: c2, c4, c5.
-__device__ __forceinline__ void soft_mask4(const float e[kCand], float inv_sum, float M[4]) {
-  M[0] = (e[0] + e[1] + e[2]) * inv_sum;
-  M[1] = (e[0] + e[3] + e[4]) * inv_sum;
-  M[2] = (e[1] + e[3] + e[5]) * inv_sum;
-  M[3] = (e[2] + e[4] + e[5]) * inv_sum;
+// Soft mask M_j = sum of p_c over the candidates keeping position j.
+__device__ __forceinline__ void soft_mask4(const float num[4], float inv_sum, float M[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) M[j] = num[j] * inv_sum;
 }
 
 // bf16 pairs packed in a 32-bit word: element 0 in the low half.

@@ -97,10 +97,10 @@ __device__ __forceinline__ void fwd_group(const FwdParams& p, const float* tab, 
                                           const float L[kCand], uint32_t w01, uint32_t w23,
                                           uint32_t& o01, uint32_t& o23, float& acc,
                                           float prob_out[kCand]) {
-  float g[kCand], e[kCand], inv, M[4];
+  float g[kCand], e[kCand], inv, num[4], M[4];
   gumbel6(group_words(gidx, p.step, p.tensor_id, p.keys), tab, g);
-  softmax6(L, g, p.kappa, p.rho, e, inv);
-  soft_mask4(e, inv, M);
+  softmax6(L, g, p.kappa, p.rho, e, inv, num);
+  soft_mask4(num, inv, M);
   const float x0 = __fmul_rn(bf16_lo(w01), M[0]);
   const float x1 = __fmul_rn(bf16_hi(w01), M[1]);
   const float x2 = __fmul_rn(bf16_lo(w23), M[2]);
@@ -204,14 +204,14 @@ template <bool kReg>
 __device__ __forceinline__ void bwd_group(const BwdParams& p, const float* tab, uint64_t gidx,
                                           const float L[kCand], uint32_t w01, uint32_t w23,
                                           uint32_t g01, uint32_t g23, float out[kCand]) {
-  float g[kCand], e[kCand], inv;
+  float g[kCand], e[kCand], inv, num[4];
   gumbel6(group_words(gidx, p.step, p.tensor_id, p.keys), tab, g);
-  softmax6(L, g, p.kappa, p.rho, e, inv);
+  softmax6(L, g, p.kappa, p.rho, e, inv, num);
   const float w[4] = {bf16_lo(w01), bf16_hi(w01), bf16_lo(w23), bf16_hi(w23)};
   float t[4] = {bf16_lo(g01), bf16_hi(g01), bf16_lo(g23), bf16_hi(g23)};
   if (kReg) {
     float M[4];
-    soft_mask4(e, inv, M);
+    soft_mask4(num, inv, M);
 #pragma unroll
     for (int j = 0; j < 4; ++j) t[j] = __fmaf_rn(p.two_reg, __fmul_rn(w[j], M[j]), t[j]);
   }

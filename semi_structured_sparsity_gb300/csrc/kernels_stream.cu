@@ -8,7 +8,7 @@
 // "Accelerating Sparse Deep Neural Networks", Sec. 3.1 (compressed 2:4
 // storage) and Sec. 4.1 (magnitude pruning).
 //
-// Structure (one CTA per SM, 1 producer warp + 16 consumer warps):
+// Structure (one CTA per SM: 1 producer warp + 16 consumer warps):
 //   * Work is a list of chunks.  A chunk is up to 1024 consecutive groups of
 //     one row, or several whole short rows (<= 1024 groups).  The chunks of a
 //     launch are those of up to 16 matrices, concatenated; CTA b takes a
@@ -16,16 +16,19 @@
 //     finished inside one CTA (its sum of squares needs no cross-CTA step)
 //     and the CTAs carry equal byte counts to within one row.
 //   * The producer warp copies each chunk's inputs (W: 8 bytes per group,
-//     logits: 24, upstream gradient: 8) from global into one of 4 shared
-//     stages with bulk copies completing on the stage's "full" mbarrier.
+//     logits: 24, upstream gradient: 8) from global into a ring of shared
+//     stages (4 stages of 32-40 KB) with bulk copies completing on the stage's
+//     "full" mbarrier.  (Deeper rings, 5-6 stages where shared memory allows,
+//     measured no faster.)
 //   * Consumer thread t owns groups 2t and 2t+1 of every chunk: it reads them
 //     from shared memory, computes, and either stores its results straight to
 //     global memory (16-byte coalesced stores) or writes them back into the
 //     stage, from where the producer bulk-stores the whole chunk.  Each
 //     consumer warp then arrives on the stage's "empty" mbarrier.
 //   * After a stage's empty barrier completes, the producer finishes that
-//     chunk: it sums the per-thread row partials in a fixed order (forward)
-//     and issues the bulk store of staged outputs, then refills the stage.
+//     chunk: it sums the per-thread row partials (left in the threads' W
+//     slots) in a fixed order (forward) and issues the bulk store of staged
+//     outputs, then refills the stage.
 //   * Every wait is bounded (pipeline.cuh).  On a timeout the CTA raises an
 //     abort flag, sets the device error word, the producer waits (bounded)
 //     for its copies still in flight, and all warps return.
@@ -39,17 +42,14 @@ __device__ __align__(16) float g_gumbel_table_s[kTableSize] = {
 #include "gumbel_table.inc"
 };
 
-// Bit 0: a consumer wait timed out; bit 1: a producer wait timed out;
-// bit 2: the final drain of in-flight copies timed out.
+// Bit 0: a consumer's wait for a stage's copies timed out; bit 1: the
+// producer's wait for a stage's release timed out; bit 2: the final drain of
+// in-flight copies timed out.
 __device__ uint32_t g_stream_error_word = 0;
 
 namespace {
 
-constexpr int kConsumerWarps = 16;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
-constexpr int kChunkGroups = 2 * kConsumers;  // 1024
-constexpr int kStages = 4;
+constexpr int kChunkGroups = 1024;           // groups per chunk
 constexpr int kMaxMats = kMaxBatch;
 
 struct MatDesc {
@@ -85,7 +85,7 @@ struct StreamParams {
   int64_t total_chunks;
   uint64_t wait_ns;        // bound of every pipeline wait
   uint64_t drain_ns;       // bound of the final wait for copies in flight
-  int32_t withhold_loads;  // test hook: the producer issues no copies
+  int32_t withhold_loads;  // test hook: no copies are issued
   Scalars s;
 };
 
@@ -181,78 +181,139 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, uint32_t b
 }
 
 // ---------------------------------------------------------------------------
-// Per-op policies.
+// Fragments: consumer thread t of a GPT-groups-per-thread kernel owns groups
+// GPT*t .. GPT*t + GPT - 1 of every chunk (8 bytes of W and 24 bytes of
+// logits per group, contiguous in the stage).
+// ---------------------------------------------------------------------------
+
+template <int GPT>
+__device__ __forceinline__ void load_w(const uint8_t* base, int t, uint32_t w[2 * GPT]) {
+  if constexpr (GPT == 2) {
+    const uint4 v = *reinterpret_cast<const uint4*>(base + 16 * t);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2*>(base + 8 * t);
+    w[0] = v.x; w[1] = v.y;
+  }
+}
+
+template <int GPT>
+__device__ __forceinline__ void load_l(const uint8_t* base, int t, float L[6 * GPT]) {
+  if constexpr (GPT == 2) {
+    const float4* q = reinterpret_cast<const float4*>(base + 48 * t);
+    const float4 a = q[0], b = q[1], c = q[2];
+    L[0] = a.x; L[1] = a.y; L[2] = a.z; L[3] = a.w; L[4] = b.x; L[5] = b.y;
+    L[6] = b.z; L[7] = b.w; L[8] = c.x; L[9] = c.y; L[10] = c.z; L[11] = c.w;
+  } else {
+    const float2* q = reinterpret_cast<const float2*>(base + 24 * t);
+    const float2 a = q[0], b = q[1], c = q[2];
+    L[0] = a.x; L[1] = a.y; L[2] = b.x; L[3] = b.y; L[4] = c.x; L[5] = c.y;
+  }
+}
+
+// 24*GPT bytes (GPT groups of six fp32 values) to shared or global memory.
+template <int GPT>
+__device__ __forceinline__ void store_l(void* base_bytes, int64_t t, const float L[6 * GPT]) {
+  if constexpr (GPT == 2) {
+    float4* q = reinterpret_cast<float4*>(static_cast<uint8_t*>(base_bytes) + 48 * t);
+    q[0] = make_float4(L[0], L[1], L[2], L[3]);
+    q[1] = make_float4(L[4], L[5], L[6], L[7]);
+    q[2] = make_float4(L[8], L[9], L[10], L[11]);
+  } else {
+    float2* q = reinterpret_cast<float2*>(static_cast<uint8_t*>(base_bytes) + 24 * t);
+    q[0] = make_float2(L[0], L[1]);
+    q[1] = make_float2(L[2], L[3]);
+    q[2] = make_float2(L[4], L[5]);
+  }
+}
+
+// 8*GPT bytes of bf16 W' words to global memory, streaming.
+template <int GPT>
+__device__ __forceinline__ void store_w_global(void* out, int64_t t, const uint32_t o[2 * GPT]) {
+  if constexpr (GPT == 2)
+    __stcs(static_cast<uint4*>(out) + t, make_uint4(o[0], o[1], o[2], o[3]));
+  else
+    __stcs(static_cast<uint2*>(out) + t, make_uint2(o[0], o[1]));
+}
+
+// ---------------------------------------------------------------------------
+// Per-op policies (GPT = groups per consumer thread).
 //   kTable      the Gumbel table is loaded into shared memory
 //   kRowSq      consumers leave per-thread row partials for the producer
 //   kStaged     consumers write the chunk's output into the stage; the
 //               producer bulk-stores it (kOutBytesPerGroup bytes per group
 //               from stage offset kOutOffset to out0)
+//   kWarpWide   consume() is called by every lane, active or not
 // ---------------------------------------------------------------------------
 
-struct PriorOp {
+template <int GPT_, int kStages_>
+struct OpBase {
+  static constexpr int kGPT = GPT_;
+  static constexpr int kConsumers = kChunkGroups / GPT_;
+  static constexpr int kConsumerWarps = kConsumers / 32;
+  static constexpr int kThreads = kConsumers + 32;   // + the producer warp
+  static constexpr int kStages = kStages_;
+  // a thread's row partial is left in its own (already read) W slot
+  static constexpr uint32_t kPartStride = 8 * GPT_;
+};
+
+template <int GPT>
+struct PriorOp : OpBase<GPT, 4> {
   static constexpr bool kTable = false, kRowSq = false, kStaged = true, kWarpWide = false;
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
   static constexpr uint32_t kOutOffset = kChunkGroups * 8;
   static constexpr uint32_t kOutBytesPerGroup = 24;
 
-  __device__ static uint32_t issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
+  __device__ static void issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
     const uint32_t wb = static_cast<uint32_t>(c.ng) * 8;
     mbar_arrive_expect_tx(bar, wb);
     bulk_load(st, static_cast<const uint8_t*>(d.W) + c.g0 * 8, wb, bar);
-    return wb;
   }
 
   __device__ static void consume(const StreamParams& p, const MatDesc&, const Chunk&, uint8_t* st,
-                                 int t, const float*, float&, float*) {
-    const uint4 w = *reinterpret_cast<const uint4*>(st + 16 * t);
-    float a[kCand], b[kCand];
+                                 int t, const float*, float&) {
+    uint32_t w[2 * GPT];
+    load_w<GPT>(st, t, w);
+    float out[6 * GPT];
     const float s = p.s.scale;
-    const float w0 = fabsf(bf16_lo(w.x)), w1 = fabsf(bf16_hi(w.x));
-    const float w2 = fabsf(bf16_lo(w.y)), w3 = fabsf(bf16_hi(w.y));
-    const float w4 = fabsf(bf16_lo(w.z)), w5 = fabsf(bf16_hi(w.z));
-    const float w6 = fabsf(bf16_lo(w.w)), w7 = fabsf(bf16_hi(w.w));
-    a[0] = __fmul_rn(s, __fadd_rn(w0, w1));
-    a[1] = __fmul_rn(s, __fadd_rn(w0, w2));
-    a[2] = __fmul_rn(s, __fadd_rn(w0, w3));
-    a[3] = __fmul_rn(s, __fadd_rn(w1, w2));
-    a[4] = __fmul_rn(s, __fadd_rn(w1, w3));
-    a[5] = __fmul_rn(s, __fadd_rn(w2, w3));
-    b[0] = __fmul_rn(s, __fadd_rn(w4, w5));
-    b[1] = __fmul_rn(s, __fadd_rn(w4, w6));
-    b[2] = __fmul_rn(s, __fadd_rn(w4, w7));
-    b[3] = __fmul_rn(s, __fadd_rn(w5, w6));
-    b[4] = __fmul_rn(s, __fadd_rn(w5, w7));
-    b[5] = __fmul_rn(s, __fadd_rn(w6, w7));
-    float4* o = reinterpret_cast<float4*>(st + kOutOffset + 48 * t);
-    o[0] = make_float4(a[0], a[1], a[2], a[3]);
-    o[1] = make_float4(a[4], a[5], b[0], b[1]);
-    o[2] = make_float4(b[2], b[3], b[4], b[5]);
+#pragma unroll
+    for (int g = 0; g < GPT; ++g) {
+      const float a0 = fabsf(bf16_lo(w[2 * g])), a1 = fabsf(bf16_hi(w[2 * g]));
+      const float a2 = fabsf(bf16_lo(w[2 * g + 1])), a3 = fabsf(bf16_hi(w[2 * g + 1]));
+      float* o = out + 6 * g;
+      o[0] = __fmul_rn(s, __fadd_rn(a0, a1));
+      o[1] = __fmul_rn(s, __fadd_rn(a0, a2));
+      o[2] = __fmul_rn(s, __fadd_rn(a0, a3));
+      o[3] = __fmul_rn(s, __fadd_rn(a1, a2));
+      o[4] = __fmul_rn(s, __fadd_rn(a1, a3));
+      o[5] = __fmul_rn(s, __fadd_rn(a2, a3));
+    }
+    store_l<GPT>(st + kOutOffset, t, out);
   }
 };
 
-template <bool kProbs>
-struct FwdOp {
+template <bool kProbs, int GPT>
+struct FwdOp : OpBase<GPT, 4> {
   static constexpr bool kTable = true, kRowSq = true, kStaged = false, kWarpWide = false;
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
   static constexpr uint32_t kOutOffset = 0;
   static constexpr uint32_t kOutBytesPerGroup = 0;
 
-  __device__ static uint32_t issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
+  __device__ static void issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
     const uint32_t wb = static_cast<uint32_t>(c.ng) * 8, lb = static_cast<uint32_t>(c.ng) * 24;
     mbar_arrive_expect_tx(bar, wb + lb);
     bulk_load(st, static_cast<const uint8_t*>(d.W) + c.g0 * 8, wb, bar);
     bulk_load(st + kChunkGroups * 8, static_cast<const uint8_t*>(d.L) + c.g0 * 24, lb, bar);
-    return wb + lb;
   }
 
   __device__ static void group(const StreamParams& p, const float* tab, uint64_t gidx,
                                uint32_t tensor_id, const float L[kCand], uint32_t w01,
                                uint32_t w23, uint32_t& o01, uint32_t& o23, float& acc,
                                float prob[kCand]) {
-    float g[kCand], e[kCand], inv, M[4];
+    float g[kCand], e[kCand], inv, num[4], M[4];
     gumbel6(group_words(gidx, p.s.step, tensor_id, p.s.keys), tab, g);
-    softmax6(L, g, p.s.kappa, p.s.rho, e, inv);
-    soft_mask4(e, inv, M);
+    softmax6(L, g, p.s.kappa, p.s.rho, e, inv, num);
+    soft_mask4(num, inv, M);
     const float x0 = __fmul_rn(bf16_lo(w01), M[0]);
     const float x1 = __fmul_rn(bf16_hi(w01), M[1]);
     const float x2 = __fmul_rn(bf16_lo(w23), M[2]);
@@ -270,57 +331,48 @@ struct FwdOp {
   }
 
   __device__ static void consume(const StreamParams& p, const MatDesc& d, const Chunk& c,
-                                 uint8_t* st, int t, const float* tab, float& acc,
-                                 float* part) {
-    const int64_t item = c.g0 / 2 + t;
-    const uint4 w = *reinterpret_cast<const uint4*>(st + 16 * t);
-    const float4* Ls = reinterpret_cast<const float4*>(st + kChunkGroups * 8 + 48 * t);
-    const float4 a = Ls[0], b = Ls[1], cc = Ls[2];
-    const float La[kCand] = {a.x, a.y, a.z, a.w, b.x, b.y};
-    const float Lb[kCand] = {b.z, b.w, cc.x, cc.y, cc.z, cc.w};
-    uint4 o;
-    float pa[kCand], pb[kCand];
-    group(p, tab, 2 * static_cast<uint64_t>(item), d.tensor_id, La, w.x, w.y, o.x, o.y, acc, pa);
-    group(p, tab, 2 * static_cast<uint64_t>(item) + 1, d.tensor_id, Lb, w.z, w.w, o.z, o.w, acc,
-          pb);
-    __stcs(static_cast<uint4*>(d.out0) + item, o);
-    if (kProbs && d.out2 != nullptr) {
-      float4* q = static_cast<float4*>(d.out2) + 3 * item;
-      q[0] = make_float4(pa[0], pa[1], pa[2], pa[3]);
-      q[1] = make_float4(pa[4], pa[5], pb[0], pb[1]);
-      q[2] = make_float4(pb[2], pb[3], pb[4], pb[5]);
-    }
-    (void)part;
+                                 uint8_t* st, int t, const float* tab, float& acc) {
+    uint32_t w[2 * GPT], o[2 * GPT];
+    float L[6 * GPT], pr[6 * GPT];
+    load_w<GPT>(st, t, w);
+    load_l<GPT>(st + kChunkGroups * 8, t, L);
+    const uint64_t g0 = static_cast<uint64_t>(c.g0) + static_cast<uint64_t>(GPT * t);
+#pragma unroll
+    for (int g = 0; g < GPT; ++g)
+      group(p, tab, g0 + g, d.tensor_id, L + 6 * g, w[2 * g], w[2 * g + 1], o[2 * g],
+            o[2 * g + 1], acc, pr + 6 * g);
+    const int64_t unit = c.g0 / GPT + t;   // this thread's GPT-group unit
+    store_w_global<GPT>(d.out0, unit, o);
+    if (kProbs && d.out2 != nullptr) store_l<GPT>(d.out2, unit, pr);
   }
 };
 
-template <bool kReg>
-struct BwdOp {
+template <bool kReg, int GPT>
+struct BwdOp : OpBase<GPT, 4> {
   static constexpr bool kTable = true, kRowSq = false, kStaged = true, kWarpWide = false;
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 8 + 24);
   static constexpr uint32_t kOutOffset = kChunkGroups * 16;
   static constexpr uint32_t kOutBytesPerGroup = 24;
 
-  __device__ static uint32_t issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
+  __device__ static void issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
     const uint32_t wb = static_cast<uint32_t>(c.ng) * 8, lb = static_cast<uint32_t>(c.ng) * 24;
     mbar_arrive_expect_tx(bar, 2 * wb + lb);
     bulk_load(st, static_cast<const uint8_t*>(d.W) + c.g0 * 8, wb, bar);
     bulk_load(st + kChunkGroups * 8, static_cast<const uint8_t*>(d.G) + c.g0 * 8, wb, bar);
     bulk_load(st + kChunkGroups * 16, static_cast<const uint8_t*>(d.L) + c.g0 * 24, lb, bar);
-    return 2 * wb + lb;
   }
 
   __device__ static void group(const StreamParams& p, const float* tab, uint64_t gidx,
                                uint32_t tensor_id, const float L[kCand], uint32_t w01,
                                uint32_t w23, uint32_t g01, uint32_t g23, float out[kCand]) {
-    float g[kCand], e[kCand], inv;
+    float g[kCand], e[kCand], inv, num[4];
     gumbel6(group_words(gidx, p.s.step, tensor_id, p.s.keys), tab, g);
-    softmax6(L, g, p.s.kappa, p.s.rho, e, inv);
+    softmax6(L, g, p.s.kappa, p.s.rho, e, inv, num);
     const float w[4] = {bf16_lo(w01), bf16_hi(w01), bf16_lo(w23), bf16_hi(w23)};
     float t[4] = {bf16_lo(g01), bf16_hi(g01), bf16_lo(g23), bf16_hi(g23)};
     if (kReg) {
       float M[4];
-      soft_mask4(e, inv, M);
+      soft_mask4(num, inv, M);
 #pragma unroll
       for (int j = 0; j < 4; ++j) t[j] = __fmaf_rn(p.s.two_reg, __fmul_rn(w[j], M[j]), t[j]);
     }
@@ -341,21 +393,18 @@ struct BwdOp {
   }
 
   __device__ static void consume(const StreamParams& p, const MatDesc& d, const Chunk& c,
-                                 uint8_t* st, int t, const float* tab, float&, float*) {
-    const int64_t item = c.g0 / 2 + t;
-    const uint4 w = *reinterpret_cast<const uint4*>(st + 16 * t);
-    const uint4 gr = *reinterpret_cast<const uint4*>(st + kChunkGroups * 8 + 16 * t);
-    float4* Ls = reinterpret_cast<float4*>(st + kChunkGroups * 16 + 48 * t);
-    const float4 a = Ls[0], b = Ls[1], cc = Ls[2];
-    const float La[kCand] = {a.x, a.y, a.z, a.w, b.x, b.y};
-    const float Lb[kCand] = {b.z, b.w, cc.x, cc.y, cc.z, cc.w};
-    float da[kCand], db[kCand];
-    group(p, tab, 2 * static_cast<uint64_t>(item), d.tensor_id, La, w.x, w.y, gr.x, gr.y, da);
-    group(p, tab, 2 * static_cast<uint64_t>(item) + 1, d.tensor_id, Lb, w.z, w.w, gr.z, gr.w, db);
-    // dlogits overwrite this thread's own logits in the stage
-    Ls[0] = make_float4(da[0], da[1], da[2], da[3]);
-    Ls[1] = make_float4(da[4], da[5], db[0], db[1]);
-    Ls[2] = make_float4(db[2], db[3], db[4], db[5]);
+                                 uint8_t* st, int t, const float* tab, float&) {
+    uint32_t w[2 * GPT], gr[2 * GPT];
+    float L[6 * GPT], dl[6 * GPT];
+    load_w<GPT>(st, t, w);
+    load_w<GPT>(st + kChunkGroups * 8, t, gr);
+    load_l<GPT>(st + kChunkGroups * 16, t, L);
+    const uint64_t g0 = static_cast<uint64_t>(c.g0) + static_cast<uint64_t>(GPT * t);
+#pragma unroll
+    for (int g = 0; g < GPT; ++g)
+      group(p, tab, g0 + g, d.tensor_id, L + 6 * g, w[2 * g], w[2 * g + 1], gr[2 * g],
+            gr[2 * g + 1], dl + 6 * g);
+    store_l<GPT>(st + kChunkGroups * 16, t, dl);   // dlogits over this thread's own logits
   }
 };
 
@@ -385,17 +434,18 @@ __device__ __forceinline__ uint32_t select4(uint32_t e0, uint32_t e1, uint32_t e
   return k == 0 ? e0 : (k == 1 ? e1 : (k == 2 ? e2 : e3));
 }
 
-struct CompressOp {
+template <int GPT>
+struct CompressOp : OpBase<GPT, 4> {
   static constexpr bool kTable = false, kRowSq = false, kStaged = false, kWarpWide = true;
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
   static constexpr uint32_t kOutOffset = 0;
   static constexpr uint32_t kOutBytesPerGroup = 0;
 
-  __device__ static uint32_t issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
-    return FwdOp<false>::issue(d, c, st, bar);
+  __device__ static void issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
+    FwdOp<false, GPT>::issue(d, c, st, bar);
   }
 
-  // Kept pair of one group: returns (w_i | w_j << 16) and sets the code.
+  // Kept pair of one group: returns (w_i | w_j << 16) and sets code and candidate.
   __device__ static uint32_t keep(const float L[kCand], uint32_t w01, uint32_t w23, uint32_t& code,
                                   uint32_t& cand) {
     const int c = first_argmax6(L);
@@ -407,32 +457,39 @@ struct CompressOp {
   }
 
   __device__ static void consume(const StreamParams&, const MatDesc& d, const Chunk& c,
-                                 uint8_t* st, int t, const float*, float&, float*) {
-    // all 32 lanes of a warp take this path together (chunks hold a multiple
-    // of 8 groups, so the 4 lanes sharing a code word are all active or not)
-    const int64_t item = c.g0 / 2 + t;
-    const bool active = 2 * t < c.ng;
-    uint32_t byte = 0;
+                                 uint8_t* st, int t, const float*, float&) {
+    // Every lane comes here.  Chunks hold a multiple of 8 groups, so the
+    // 8/GPT lanes that share one 32-bit code word are all active or all not.
+    constexpr int kLanesPerWord = 8 / GPT;
+    const int64_t unit = c.g0 / GPT + t;
+    const bool active = GPT * t < c.ng;
+    uint32_t codes = 0;
     if (active) {
-      const uint4 w = *reinterpret_cast<const uint4*>(st + 16 * t);
-      const float4* Ls = reinterpret_cast<const float4*>(st + kChunkGroups * 8 + 48 * t);
-      const float4 a = Ls[0], b = Ls[1], cc = Ls[2];
-      const float La[kCand] = {a.x, a.y, a.z, a.w, b.x, b.y};
-      const float Lb[kCand] = {b.z, b.w, cc.x, cc.y, cc.z, cc.w};
-      uint32_t ca, cb, ka, kb;
-      const uint32_t va = keep(La, w.x, w.y, ca, ka);
-      const uint32_t vb = keep(Lb, w.z, w.w, cb, kb);
-      __stcs(static_cast<uint2*>(d.out0) + item, make_uint2(va, vb));
-      byte = ca | (cb << 4);
-      if (d.out2 != nullptr)
-        static_cast<uint16_t*>(d.out2)[item] = static_cast<uint16_t>(ka | (kb << 8));
+      uint32_t w[2 * GPT], v[GPT], cand[GPT];
+      float L[6 * GPT];
+      load_w<GPT>(st, t, w);
+      load_l<GPT>(st + kChunkGroups * 8, t, L);
+#pragma unroll
+      for (int g = 0; g < GPT; ++g) {
+        uint32_t code;
+        v[g] = keep(L + 6 * g, w[2 * g], w[2 * g + 1], code, cand[g]);
+        codes |= code << (4 * g);
+      }
+      if constexpr (GPT == 2) {
+        __stcs(static_cast<uint2*>(d.out0) + unit, make_uint2(v[0], v[1]));
+        if (d.out2 != nullptr)
+          static_cast<uint16_t*>(d.out2)[unit] = static_cast<uint16_t>(cand[0] | (cand[1] << 8));
+      } else {
+        __stcs(static_cast<uint32_t*>(d.out0) + unit, v[0]);
+        if (d.out2 != nullptr) static_cast<uint8_t*>(d.out2)[unit] = static_cast<uint8_t>(cand[0]);
+      }
     }
-    // four consecutive lanes hold the 8 codes of one 32-bit metadata word
     const int lane = t & 31;
-    uint32_t word = byte << (8 * (lane & 3));
-    word |= __shfl_down_sync(0xFFFFFFFFu, word, 1);
-    word |= __shfl_down_sync(0xFFFFFFFFu, word, 2);
-    if (active && (lane & 3) == 0) __stcs(static_cast<uint32_t*>(d.out1) + item / 4, word);
+    uint32_t word = codes << (4 * GPT * (lane % kLanesPerWord));
+#pragma unroll
+    for (int o = 1; o < kLanesPerWord; o <<= 1) word |= __shfl_down_sync(0xFFFFFFFFu, word, o);
+    if (active && lane % kLanesPerWord == 0)
+      __stcs(static_cast<uint32_t*>(d.out1) + unit / kLanesPerWord, word);
   }
 };
 
@@ -444,22 +501,21 @@ template <class Op>
 struct Layout {
   static constexpr uint32_t kTableBytes = Op::kTable ? kTableSize * 4 : 0;
   static constexpr uint32_t kStageOff = kTableBytes;
-  static constexpr uint32_t kPartOff = kStageOff + kStages * Op::kStageBytes;
-  static constexpr uint32_t kPartBytes = Op::kRowSq ? kStages * kConsumers * 4 : 0;
-  static constexpr uint32_t kBarOff = kPartOff + kPartBytes;
-  static constexpr uint32_t kChunkOff = kBarOff + 2 * kStages * 8;
-  static constexpr uint32_t kFlagOff = kChunkOff + kStages * sizeof(Chunk);
+  static constexpr uint32_t kBarOff = kStageOff + Op::kStages * Op::kStageBytes;
+  static constexpr uint32_t kChunkOff = kBarOff + 2 * Op::kStages * 8;
+  static constexpr uint32_t kFlagOff = kChunkOff + Op::kStages * sizeof(Chunk);
   static constexpr uint32_t kBytes = kFlagOff + 16;
 };
 
+// Producer warp: refills the stage ring, finishes retired chunks.
 template <class Op>
 __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64_t u1) {
   using Lay = Layout<Op>;
+  constexpr int S = Op::kStages;
   const int lane = threadIdx.x & 31;
   uint8_t* stages = smem + Lay::kStageOff;
-  const float* part = reinterpret_cast<const float*>(smem + Lay::kPartOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
-  uint64_t* empty = full + kStages;
+  uint64_t* empty = full + S;
   Chunk* held = reinterpret_cast<Chunk*>(smem + Lay::kChunkOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kFlagOff);
 
@@ -467,19 +523,22 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
   auto retire = [&](int s) {
     const Chunk c = held[s];
     const MatDesc& d = p.mats[c.mat];
+    const uint8_t* st = stages + s * Op::kStageBytes;
     if (Op::kRowSq && d.out1 != nullptr && c.nrows > 0) {
-      const float* ps = part + s * kConsumers;
       float* row_sq = static_cast<float*>(d.out1);
+      auto part = [&](int k) {
+        return *reinterpret_cast<const float*>(st + k * Op::kPartStride);
+      };
       if (d.cpr > 0) {
         float v = 0.f;
-        for (int k = lane; k < kConsumers; k += 32) v += ps[k];
+        for (int k = lane; k < Op::kConsumers; k += 32) v += part(k);
         v = warp_sum(v);
         if (lane == 0) row_sq[c.row0] = v;
       } else {
-        const int ipr = d.gpr / 2;
+        const int tpr = d.gpr / Op::kGPT;   // threads per short row
         for (int r = 0; r < c.nrows; ++r) {
           float v = 0.f;
-          for (int k = lane; k < ipr; k += 32) v += ps[r * ipr + k];
+          for (int k = lane; k < tpr; k += 32) v += part(r * tpr + k);
           v = warp_sum(v);
           if (lane == 0) row_sq[c.row0 + r] = v;
         }
@@ -487,8 +546,7 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
     }
     if (Op::kStaged && lane == 0) {
       bulk_store(static_cast<uint8_t*>(d.out0) + c.g0 * Op::kOutBytesPerGroup,
-                 stages + s * Op::kStageBytes + Op::kOutOffset,
-                 static_cast<uint32_t>(c.ng) * Op::kOutBytesPerGroup);
+                 st + Op::kOutOffset, static_cast<uint32_t>(c.ng) * Op::kOutBytesPerGroup);
       bulk_commit();
     }
   };
@@ -498,10 +556,10 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
   Chunk c;
   int64_t n = 0;
   bool ok = true;
-  while (ok && it.next(c)) {
-    const int s = static_cast<int>(n % kStages);
-    if (n >= kStages) {
-      const bool got = mbar_wait_bounded(&empty[s], static_cast<uint32_t>((n / kStages - 1) & 1),
+  while (it.next(c)) {
+    const int s = static_cast<int>(n % S);
+    if (n >= S) {
+      const bool got = mbar_wait_bounded(&empty[s], static_cast<uint32_t>((n / S - 1) & 1),
                                          p.wait_ns, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) {
         if (lane == 0) raise_abort(abort_flag, 2u);
@@ -514,16 +572,15 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
     }
     if (lane == 0) held[s] = c;
     __syncwarp();
-    if (lane == 0 && !p.withhold_loads) Op::issue(p.mats[c.mat], c, stages + s * Op::kStageBytes,
-                                                  &full[s]);
+    if (lane == 0 && !p.withhold_loads)
+      Op::issue(p.mats[c.mat], c, stages + s * Op::kStageBytes, &full[s]);
     ++n;
   }
   if (ok) {
-    // drain: finish the last chunks as their consumers release them
-    const int64_t first = n > kStages ? n - kStages : 0;
-    for (int64_t k = first; k < n; ++k) {
-      const int s = static_cast<int>(k % kStages);
-      const bool got = mbar_wait_bounded(&empty[s], static_cast<uint32_t>((k / kStages) & 1),
+    // drain: finish the last chunks as the consumers release them
+    for (int64_t k = n > S ? n - S : 0; k < n; ++k) {
+      const int s = static_cast<int>(k % S);
+      const bool got = mbar_wait_bounded(&empty[s], static_cast<uint32_t>((k / S) & 1),
                                          p.wait_ns, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) {
         if (lane == 0) raise_abort(abort_flag, 2u);
@@ -536,29 +593,28 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
   }
   if (!ok && !p.withhold_loads) {
     // aborted: wait (bounded) for every copy still landing in shared memory
-    const int64_t first = n > kStages ? n - kStages : 0;
-    for (int64_t k = first; k < n; ++k) {
-      const int s = static_cast<int>(k % kStages);
+    for (int64_t k = n > S ? n - S : 0; k < n; ++k) {
+      const int s = static_cast<int>(k % S);
       int never = 0;
-      if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((k / kStages) & 1), p.drain_ns,
-                             &never)) {
-        if (lane == 0) atomicOr(&g_stream_error_word, 4u);
-      }
+      const bool landed = mbar_wait_bounded(&full[s], static_cast<uint32_t>((k / S) & 1),
+                                            p.drain_ns, &never);
+      if (!landed && lane == 0) atomicOr(&g_stream_error_word, 4u);
     }
   }
   if (Op::kStaged && lane == 0) bulk_wait_all();
 }
 
+// Consumer warps: thread t owns GPT groups of every chunk.
 template <class Op>
 __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64_t u1) {
   using Lay = Layout<Op>;
+  constexpr int S = Op::kStages;
   const int t = threadIdx.x - 32;
   const int lane = threadIdx.x & 31;
   uint8_t* stages = smem + Lay::kStageOff;
-  float* part = reinterpret_cast<float*>(smem + Lay::kPartOff);
   const float* tab = reinterpret_cast<const float*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
-  uint64_t* empty = full + kStages;
+  uint64_t* empty = full + S;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kFlagOff);
 
   ChunkIter it;
@@ -567,9 +623,9 @@ __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
   int64_t n = 0;
   float acc = 0.f;
   while (it.next(c)) {
-    const int s = static_cast<int>(n % kStages);
-    const bool got = mbar_wait_bounded(&full[s], static_cast<uint32_t>((n / kStages) & 1),
-                                       p.wait_ns, abort_flag);
+    const int s = static_cast<int>(n % S);
+    const bool got = mbar_wait_bounded(&full[s], static_cast<uint32_t>((n / S) & 1), p.wait_ns,
+                                       abort_flag);
     if (!__all_sync(0xFFFFFFFFu, got)) {
       if (lane == 0) raise_abort(abort_flag, 1u);
       break;
@@ -577,18 +633,19 @@ __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
     const MatDesc& d = p.mats[c.mat];
     uint8_t* st = stages + s * Op::kStageBytes;
     if (Op::kWarpWide)
-      Op::consume(p, d, c, st, t, tab, acc, part);   // every lane, active or not
-    else if (2 * t < c.ng)
-      Op::consume(p, d, c, st, t, tab, acc, part);
+      Op::consume(p, d, c, st, t, tab, acc);   // every lane, active or not
+    else if (Op::kGPT * t < c.ng)
+      Op::consume(p, d, c, st, t, tab, acc);
     if (Op::kRowSq) {
-      float* ps = part + s * kConsumers;
+      // the row partial goes into this thread's own W slot, already read
+      float* part = reinterpret_cast<float*>(st + t * Op::kPartStride);
       if (d.cpr > 0) {
         if (c.nrows > 0) {
-          ps[t] = acc;   // the row ends in this chunk
+          *part = acc;   // the row ends in this chunk
           acc = 0.f;
         }
       } else {
-        ps[t] = acc;     // short rows: one item per thread per chunk
+        *part = acc;     // short rows: each thread's groups lie in one row
         acc = 0.f;
       }
     }
@@ -600,19 +657,20 @@ __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
 }
 
 template <class Op>
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ StreamParams p) {
+__global__ void __launch_bounds__(Op::kThreads, 1)
+    stream_kernel(const __grid_constant__ StreamParams p) {
   using Lay = Layout<Op>;
   extern __shared__ __align__(128) uint8_t smem[];
   if (Op::kTable) {
     const float4* src = reinterpret_cast<const float4*>(g_gumbel_table_s);
     float4* dst = reinterpret_cast<float4*>(smem);
-    for (int i = threadIdx.x; i < kTableSize / 4; i += kThreads) dst[i] = src[i];
+    for (int i = threadIdx.x; i < kTableSize / 4; i += Op::kThreads) dst[i] = src[i];
   }
   if (threadIdx.x == 0) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars[s], 1);                           // full: producer's expect_tx
-      mbar_init(&bars[kStages + s], kConsumerWarps);    // empty: one arrive per consumer warp
+    for (int s = 0; s < Op::kStages; ++s) {
+      mbar_init(&bars[s], 1);                                  // full: producer's expect_tx
+      mbar_init(&bars[Op::kStages + s], Op::kConsumerWarps);   // empty: one per consumer warp
     }
     *reinterpret_cast<volatile int*>(smem + Lay::kFlagOff) = 0;
     fence_barrier_init();
@@ -675,7 +733,7 @@ cudaError_t launch(const Device& dev, const StreamParams& p, cudaStream_t s) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   const int64_t grid = p.total_units < dev.num_sms ? p.total_units : dev.num_sms;
-  stream_kernel<Op><<<static_cast<int>(grid), kThreads, bytes, s>>>(p);
+  stream_kernel<Op><<<static_cast<int>(grid), Op::kThreads, bytes, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -693,8 +751,11 @@ Scalars scalars(float tau, float kappa, RngArgs rng, float reg, float scale) {
 
 }  // namespace
 
-static_assert(Layout<FwdOp<true>>::kBytes <= 232448, "forward shared memory");
-static_assert(Layout<BwdOp<true>>::kBytes <= 232448, "backward shared memory");
+constexpr int kGPT = 2;   // groups per consumer thread (16 consumer warps)
+static_assert(Layout<FwdOp<true, kGPT>>::kBytes <= 232448, "forward shared memory");
+static_assert(Layout<BwdOp<true, kGPT>>::kBytes <= 232448, "backward shared memory");
+static_assert(Layout<PriorOp<kGPT>>::kBytes <= 232448, "prior shared memory");
+static_assert(Layout<CompressOp<kGPT>>::kBytes <= 232448, "compress shared memory");
 static_assert(sizeof(StreamParams) <= 4000, "kernel parameters");
 
 cudaError_t stream_prior_init(const Device& d, const StreamMatrix* m, int n, float scale,
@@ -702,7 +763,7 @@ cudaError_t stream_prior_init(const Device& d, const StreamMatrix* m, int n, flo
   StreamParams p;
   describe(p, m, n);
   p.s = scalars(1.0f, 0.0f, {0, 0, 0}, 0.0f, scale);
-  return launch<PriorOp>(d, p, s);
+  return launch<PriorOp<kGPT>>(d, p, s);
 }
 
 cudaError_t stream_forward(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
@@ -710,7 +771,7 @@ cudaError_t stream_forward(const Device& d, const StreamMatrix* m, int n, float 
   StreamParams p;
   describe(p, m, n);
   p.s = scalars(tau, kappa, rng, 0.0f, 0.0f);
-  return probs ? launch<FwdOp<true>>(d, p, s) : launch<FwdOp<false>>(d, p, s);
+  return probs ? launch<FwdOp<true, kGPT>>(d, p, s) : launch<FwdOp<false, kGPT>>(d, p, s);
 }
 
 cudaError_t stream_backward(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
@@ -718,14 +779,15 @@ cudaError_t stream_backward(const Device& d, const StreamMatrix* m, int n, float
   StreamParams p;
   describe(p, m, n);
   p.s = scalars(tau, kappa, rng, reg_coeff, 0.0f);
-  return reg_coeff != 0.0f ? launch<BwdOp<true>>(d, p, s) : launch<BwdOp<false>>(d, p, s);
+  return reg_coeff != 0.0f ? launch<BwdOp<true, kGPT>>(d, p, s)
+                           : launch<BwdOp<false, kGPT>>(d, p, s);
 }
 
 cudaError_t stream_hard_compress(const Device& d, const StreamMatrix* m, int n, cudaStream_t s) {
   StreamParams p;
   describe(p, m, n);
   p.s = scalars(1.0f, 0.0f, {0, 0, 0}, 0.0f, 0.0f);
-  return launch<CompressOp>(d, p, s);
+  return launch<CompressOp<kGPT>>(d, p, s);
 }
 
 void stream_set_wait_ns(uint64_t ns) { g_wait_ns = ns; }

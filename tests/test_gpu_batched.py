@@ -136,10 +136,13 @@ for i, (r, c) in enumerate({shapes!r}):
 """
 
 
-def test_direct_kernels_match_oracle(tmp_path):
+@pytest.mark.parametrize("variant", [{"MASKLLM_KERNELS": "direct"}], ids=["direct"])
+def test_kernel_variants_match_oracle(tmp_path, variant):
+    """The per-matrix direct-load kernels (selected by environment, read once
+    per process) compute the same results."""
     shapes = [(7, 160), (33, 11008), (256, 1024), (300, 64)]
     script = _DIRECT_SCRIPT.format(root=ROOT, shapes=shapes, tmp=str(tmp_path))
-    env = dict(os.environ, MASKLLM_KERNELS="direct")
+    env = dict(os.environ, **variant)
     r = subprocess.run([sys.executable, "-c", script], env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
