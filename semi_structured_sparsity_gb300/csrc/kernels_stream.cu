@@ -260,13 +260,14 @@ struct OpBase {
 template <int GPT>
 struct PriorOp : OpBase<GPT, 4> {
   static constexpr bool kTable = false, kRowSq = false, kStaged = true, kWarpWide = false;
+  static constexpr bool kOutOverlapsInput = false;   // W in, logits out: separate regions
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
   static constexpr uint32_t kOutOffset = kChunkGroups * 8;
   static constexpr uint32_t kOutBytesPerGroup = 24;
 
   __device__ static void issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
     const uint32_t wb = static_cast<uint32_t>(c.ng) * 8;
-    mbar_arrive_expect_tx(bar, wb);
+    mbar_expect_tx(bar, wb);
     bulk_load(st, static_cast<const uint8_t*>(d.W) + c.g0 * 8, wb, bar);
   }
 
@@ -295,13 +296,14 @@ struct PriorOp : OpBase<GPT, 4> {
 template <bool kProbs, int GPT>
 struct FwdOp : OpBase<GPT, 4> {
   static constexpr bool kTable = true, kRowSq = true, kStaged = false, kWarpWide = false;
+  static constexpr bool kOutOverlapsInput = false;
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
   static constexpr uint32_t kOutOffset = 0;
   static constexpr uint32_t kOutBytesPerGroup = 0;
 
   __device__ static void issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
     const uint32_t wb = static_cast<uint32_t>(c.ng) * 8, lb = static_cast<uint32_t>(c.ng) * 24;
-    mbar_arrive_expect_tx(bar, wb + lb);
+    mbar_expect_tx(bar, wb + lb);
     bulk_load(st, static_cast<const uint8_t*>(d.W) + c.g0 * 8, wb, bar);
     bulk_load(st + kChunkGroups * 8, static_cast<const uint8_t*>(d.L) + c.g0 * 24, lb, bar);
   }
@@ -350,13 +352,14 @@ struct FwdOp : OpBase<GPT, 4> {
 template <bool kReg, int GPT>
 struct BwdOp : OpBase<GPT, 4> {
   static constexpr bool kTable = true, kRowSq = false, kStaged = true, kWarpWide = false;
+  static constexpr bool kOutOverlapsInput = true;    // dlogits overwrite the logits
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 8 + 24);
   static constexpr uint32_t kOutOffset = kChunkGroups * 16;
   static constexpr uint32_t kOutBytesPerGroup = 24;
 
   __device__ static void issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
     const uint32_t wb = static_cast<uint32_t>(c.ng) * 8, lb = static_cast<uint32_t>(c.ng) * 24;
-    mbar_arrive_expect_tx(bar, 2 * wb + lb);
+    mbar_expect_tx(bar, 2 * wb + lb);
     bulk_load(st, static_cast<const uint8_t*>(d.W) + c.g0 * 8, wb, bar);
     bulk_load(st + kChunkGroups * 8, static_cast<const uint8_t*>(d.G) + c.g0 * 8, wb, bar);
     bulk_load(st + kChunkGroups * 16, static_cast<const uint8_t*>(d.L) + c.g0 * 24, lb, bar);
@@ -408,35 +411,35 @@ struct BwdOp : OpBase<GPT, 4> {
   }
 };
 
-// Candidate c's kept positions and metadata code, one nibble per candidate:
+// Candidate c's metadata code i | j << 2 (one nibble per candidate) and the
+// byte selector that gathers its kept pair (i, j) out of the group's 8 bytes
+// (16 bits per candidate; byte k of the result takes source byte nibble k):
 // c0 (0,1) c1 (0,2) c2 (0,3) c3 (1,2) c4 (1,3) c5 (2,3).
-constexpr uint32_t kPairI = 0x211000u;
-constexpr uint32_t kPairJ = 0x332321u;
 constexpr uint32_t kCode = 0xED9C84u;
+constexpr uint64_t kGather03 = 0x5432761054103210ull;   // c0 .. c3
+constexpr uint32_t kGather45 = 0x76547632u;             // c4, c5
 
+// Hard-mask candidate: the first maximum of the raw logits.  fmaxf ignores a
+// NaN operand, so m is the largest non-NaN logit (NaN only if all six are);
+// the first c with L_c == m is the lowest index among the maxima (-0 == +0);
+// when every logit is NaN no comparison holds and candidate 0 is chosen.
 __device__ __forceinline__ int first_argmax6(const float L[kCand]) {
-  int best = 0;
-  float bv = L[0];
-  bool bnan = isnan(L[0]);
+  const float m = fmaxf(fmaxf(fmaxf(L[0], L[1]), fmaxf(L[2], L[3])), fmaxf(L[4], L[5]));
+  uint32_t hit = 0;
 #pragma unroll
-  for (int c = 1; c < kCand; ++c) {
-    if (!isnan(L[c]) && (bnan || L[c] > bv)) {
-      best = c;
-      bv = L[c];
-      bnan = false;
-    }
-  }
-  return best;
+  for (int c = 0; c < kCand; ++c) hit |= static_cast<uint32_t>(L[c] == m) << c;
+  return hit ? __ffs(hit) - 1 : 0;
 }
 
-__device__ __forceinline__ uint32_t select4(uint32_t e0, uint32_t e1, uint32_t e2, uint32_t e3,
-                                            uint32_t k) {
-  return k == 0 ? e0 : (k == 1 ? e1 : (k == 2 ? e2 : e3));
+__device__ __forceinline__ uint32_t gather_selector(int c) {
+  return c < 4 ? static_cast<uint32_t>(kGather03 >> (16 * c)) & 0xFFFFu
+               : (kGather45 >> (16 * (c - 4))) & 0xFFFFu;
 }
 
 template <int GPT>
 struct CompressOp : OpBase<GPT, 4> {
   static constexpr bool kTable = false, kRowSq = false, kStaged = false, kWarpWide = true;
+  static constexpr bool kOutOverlapsInput = false;
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
   static constexpr uint32_t kOutOffset = 0;
   static constexpr uint32_t kOutBytesPerGroup = 0;
@@ -445,18 +448,7 @@ struct CompressOp : OpBase<GPT, 4> {
     FwdOp<false, GPT>::issue(d, c, st, bar);
   }
 
-  // Kept pair of one group: returns (w_i | w_j << 16) and sets code and candidate.
-  __device__ static uint32_t keep(const float L[kCand], uint32_t w01, uint32_t w23, uint32_t& code,
-                                  uint32_t& cand) {
-    const int c = first_argmax6(L);
-    const uint32_t i = (kPairI >> (4 * c)) & 0xFu, j = (kPairJ >> (4 * c)) & 0xFu;
-    const uint32_t e0 = w01 & 0xFFFFu, e1 = w01 >> 16, e2 = w23 & 0xFFFFu, e3 = w23 >> 16;
-    code = (kCode >> (4 * c)) & 0xFu;
-    cand = static_cast<uint32_t>(c);
-    return select4(e0, e1, e2, e3, i) | (select4(e0, e1, e2, e3, j) << 16);
-  }
-
-  __device__ static void consume(const StreamParams&, const MatDesc& d, const Chunk& c,
+  __device__ static void consume(const StreamParams&, const MatDesc& k, const Chunk& c,
                                  uint8_t* st, int t, const float*, float&) {
     // Every lane comes here.  Chunks hold a multiple of 8 groups, so the
     // 8/GPT lanes that share one 32-bit code word are all active or all not.
@@ -471,17 +463,18 @@ struct CompressOp : OpBase<GPT, 4> {
       load_l<GPT>(st + kChunkGroups * 8, t, L);
 #pragma unroll
       for (int g = 0; g < GPT; ++g) {
-        uint32_t code;
-        v[g] = keep(L + 6 * g, w[2 * g], w[2 * g + 1], code, cand[g]);
-        codes |= code << (4 * g);
+        const int c = first_argmax6(L + 6 * g);
+        v[g] = __byte_perm(w[2 * g], w[2 * g + 1], gather_selector(c));
+        codes |= ((kCode >> (4 * c)) & 0xFu) << (4 * g);
+        cand[g] = static_cast<uint32_t>(c);
       }
       if constexpr (GPT == 2) {
-        __stcs(static_cast<uint2*>(d.out0) + unit, make_uint2(v[0], v[1]));
-        if (d.out2 != nullptr)
-          static_cast<uint16_t*>(d.out2)[unit] = static_cast<uint16_t>(cand[0] | (cand[1] << 8));
+        __stcs(static_cast<uint2*>(k.out0) + unit, make_uint2(v[0], v[1]));
+        if (k.out2 != nullptr)
+          static_cast<uint16_t*>(k.out2)[unit] = static_cast<uint16_t>(cand[0] | (cand[1] << 8));
       } else {
-        __stcs(static_cast<uint32_t*>(d.out0) + unit, v[0]);
-        if (d.out2 != nullptr) static_cast<uint8_t*>(d.out2)[unit] = static_cast<uint8_t>(cand[0]);
+        __stcs(static_cast<uint32_t*>(k.out0) + unit, v[0]);
+        if (k.out2 != nullptr) static_cast<uint8_t*>(k.out2)[unit] = static_cast<uint8_t>(cand[0]);
       }
     }
     const int lane = t & 31;
@@ -489,7 +482,7 @@ struct CompressOp : OpBase<GPT, 4> {
 #pragma unroll
     for (int o = 1; o < kLanesPerWord; o <<= 1) word |= __shfl_down_sync(0xFFFFFFFFu, word, o);
     if (active && lane % kLanesPerWord == 0)
-      __stcs(static_cast<uint32_t*>(d.out1) + unit / kLanesPerWord, word);
+      __stcs(static_cast<uint32_t*>(k.out1) + unit / kLanesPerWord, word);
   }
 };
 
@@ -568,12 +561,20 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
       }
       retire(s);
       __syncwarp();
-      if (Op::kStaged && lane == 0) bulk_wait_reads();  // stage s is about to be refilled
     }
-    if (lane == 0) held[s] = c;
+    if (lane == 0) {
+      held[s] = c;
+      // a staged store may still be reading this stage's output region:
+      // wait before the refill if the copies land there, after it if not
+      if (Op::kStaged && Op::kOutOverlapsInput) bulk_wait_reads();
+      if (!p.withhold_loads)
+        Op::issue(p.mats[c.mat], c, stages + s * Op::kStageBytes, &full[s]);
+      else
+        mbar_expect_tx(&full[s], 16);   // test hook: bytes that never come
+      if (Op::kStaged && !Op::kOutOverlapsInput) bulk_wait_reads();
+      mbar_arrive(&full[s]);   // with the copies' bytes, completes the phase
+    }
     __syncwarp();
-    if (lane == 0 && !p.withhold_loads)
-      Op::issue(p.mats[c.mat], c, stages + s * Op::kStageBytes, &full[s]);
     ++n;
   }
   if (ok) {
