@@ -79,7 +79,14 @@ def lib():
         L.orc_decompress.restype = None
         L.orc_compressed_bytes.argtypes = [i64, i64, i64]
         L.orc_compressed_bytes.restype = i64
-        _ = u8p
+        i64p = np.ctypeslib.ndpointer(np.int64, flags="C_CONTIGUOUS")
+        L.orc_candidate_of_code.argtypes = [u32]
+        L.orc_candidate_of_code.restype = C.c_int
+        L.orc_prior_from_mask.argtypes = [u32p, i64, i64, f32, f32, f32p]
+        L.orc_prior_from_mask.restype = None
+        L.orc_mask_stats.argtypes = [f32p, i64, i64, i64, f32, f32, u64, u32, u32, vp, vp, vp, vp]
+        L.orc_mask_stats.restype = None
+        _ = (u8p, i64p)
         _lib = L
     return _lib
 
@@ -224,3 +231,26 @@ def decompress(vals, meta, rows: int, cols: int):
 
 def compressed_bytes(rows: int, cols: int, elem_bytes: int) -> int:
     return int(lib().orc_compressed_bytes(rows, cols, elem_bytes))
+
+
+def candidate_of_code(code: int) -> int:
+    return int(lib().orc_candidate_of_code(code))
+
+
+def prior_from_mask(meta, rows: int, cols: int, high: float, low: float):
+    out = np.zeros((rows, cols // 4, NCAND), np.float32)
+    lib().orc_prior_from_mask(_c(meta, np.uint32).reshape(rows, cols // 32), rows, cols, high, low,
+                              out)
+    return out
+
+
+def mask_stats(L, rows, cols, tau, kappa, seed, step=0, tensor_id=0, prev_idx=None, row_begin=0):
+    """Returns (idx u8 [rows, cols/4], l1 int64 [rows] or None, maxprob f64 [rows])."""
+    L = _c(L, np.float32).reshape(rows, cols // 4, NCAND)
+    idx = np.zeros((rows, cols // 4), np.uint8)
+    l1 = np.zeros(rows, np.int64) if prev_idx is not None else None
+    mp = np.zeros(rows, np.float64)
+    prev = None if prev_idx is None else _c(prev_idx, np.uint8).reshape(rows, cols // 4)
+    lib().orc_mask_stats(L, rows, cols, row_begin, tau, kappa, seed, step, tensor_id, _ptr(prev),
+                         _ptr(idx), _ptr(l1), _ptr(mp))
+    return idx, l1, mp

@@ -453,3 +453,83 @@ void orc_decompress(const uint16_t* values, const uint32_t* meta, int64_t rows,
 int64_t orc_compressed_bytes(int64_t rows, int64_t cols, int64_t elem_bytes) {
   return rows * (cols / 2) * elem_bytes + rows * (cols / 4) / 2;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Prior from a given mask and the convergence diagnostics.                   */
+/* ------------------------------------------------------------------------ */
+
+/* The candidate whose kept pair (i, j) has metadata code i | j << 2, or -1
+ * for a code that names no candidate. */
+int orc_candidate_of_code(uint32_t code) {
+  for (int c = 0; c < ORC_NCAND; ++c)
+    if ((uint32_t)(ORC_PAIR[c][0] | (ORC_PAIR[c][1] << 2)) == code) return c;
+  return -1;
+}
+
+/* Logits that start from a given mask [MaskLLM Table 2: learned masks use a
+ * prior mask for initialisation; transfer of masks across tasks]: for every
+ * group, `high` on the candidate its 4-bit code names and `low` on the other
+ * five; a code naming no candidate gives `low` everywhere.  meta is the 2:4
+ * metadata layout of orc_hard_compress. */
+void orc_prior_from_mask(const uint32_t* meta, int64_t rows, int64_t cols, float high,
+                         float low, float* logits) {
+  const int64_t gpr = cols / 4;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t k = 0; k < gpr; ++k) {
+      const uint32_t code = (meta[r * (cols / 32) + k / 8] >> (4 * (k % 8))) & 0xFu;
+      const int c_prior = orc_candidate_of_code(code);
+      for (int c = 0; c < ORC_NCAND; ++c)
+        logits[(r * gpr + k) * ORC_NCAND + c] = (c == c_prior) ? high : low;
+    }
+}
+
+/* Convergence diagnostics of one step [MaskLLM Fig. 5: (a) the L1 distance
+ * of sampled masks between adjacent training steps; (b) the maximum
+ * probability of the mask distribution; kappa sets the randomness].
+ *   sample   the candidate drawn at this step: the first maximum of the noisy
+ *            logits z (fp32, as in orc_group_probs) -- the mask the soft mask
+ *            tends to as tau -> 0;
+ *   l1       per row, sum over groups of |S_sample - S_prev|_1 (0, 2 or 4 per
+ *            group) against the previous step's samples prev_idx (nullable:
+ *            then l1 is not computed);
+ *   maxprob  per row, sum over groups of max_c softmax(fl32(kappa * L))_c,
+ *            the categorical distribution the draw samples from (no noise).
+ * Outputs: idx_out u8 [rows, cols/4] (nullable), l1_row int64 [rows]
+ * (nullable), maxprob_row double [rows] (nullable). */
+void orc_mask_stats(const float* logits, int64_t rows, int64_t cols, int64_t row_begin,
+                    float tau, float kappa, uint64_t seed, uint32_t step, uint32_t tensor_id,
+                    const uint8_t* prev_idx, uint8_t* idx_out, int64_t* l1_row,
+                    double* maxprob_row) {
+  const float* table = orc_table();
+  const int64_t gpr = cols / 4;
+  for (int64_t r = 0; r < rows; ++r) {
+    int64_t l1 = 0;
+    double mp = 0.0;
+    for (int64_t k = 0; k < gpr; ++k) {
+      const uint64_t group = (uint64_t)((row_begin + r) * gpr + k);
+      const float* L = logits + (r * gpr + k) * ORC_NCAND;
+      float g[ORC_NCAND];
+      orc_group_noise(table, seed, step, tensor_id, group, g);
+      double p[ORC_NCAND], z[ORC_NCAND];
+      orc_group_probs(L, g, kappa, tau, 0, p, z);
+      int s = 0;
+      for (int c = 1; c < ORC_NCAND; ++c)
+        if (z[c] > z[s]) s = c;
+      if (idx_out) idx_out[r * gpr + k] = (uint8_t)s;
+      if (prev_idx) {
+        const int q = prev_idx[r * gpr + k];
+        for (int j = 0; j < 4; ++j) l1 += orc_candidate_keeps(s, j) != orc_candidate_keeps(q, j);
+      }
+      double y[ORC_NCAND], m = -INFINITY, sum = 0.0;
+      for (int c = 0; c < ORC_NCAND; ++c) {
+        float a = kappa * L[c];
+        y[c] = (double)a;
+        if (y[c] > m) m = y[c];
+      }
+      for (int c = 0; c < ORC_NCAND; ++c) sum += exp(y[c] - m);
+      mp += 1.0 / sum;   /* the largest term is exp(0) = 1 */
+    }
+    if (l1_row) l1_row[r] = l1;
+    if (maxprob_row) maxprob_row[r] = mp;
+  }
+}

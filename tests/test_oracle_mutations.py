@@ -49,6 +49,12 @@ MUTATIONS = {
                   "const double dz_dlogit = exact ? (double)kappa * (double)tau"),
     "storage_bytes": ("return rows * (cols / 2) * elem_bytes + rows * (cols / 4) / 2;",
                       "return rows * (cols / 2) * elem_bytes + rows * (cols / 4);"),
+    "code_to_candidate": ("if ((uint32_t)(ORC_PAIR[c][0] | (ORC_PAIR[c][1] << 2)) == code) return c;",
+                          "if ((uint32_t)(ORC_PAIR[c][1] | (ORC_PAIR[c][0] << 2)) == code) return c;"),
+    "stats_l1": ("for (int j = 0; j < 4; ++j) l1 += orc_candidate_keeps(s, j) != orc_candidate_keeps(q, j);",
+                 "for (int j = 0; j < 4; ++j) l1 += orc_candidate_keeps(s, j) != orc_candidate_keeps(s, j);"),
+    "stats_maxprob_kappa": ("        float a = kappa * L[c];\n        y[c] = (double)a;",
+                            "        float a = L[c];\n        y[c] = (double)a;"),
 }
 
 

@@ -461,3 +461,95 @@ def test_storage_savings_match_the_page(orc):
     # the exact closed forms: 16-bit -> 56.25% of dense, 8-bit -> 62.5%
     assert orc.compressed_bytes(64, 64, 2) * 10000 == 5625 * 64 * 64 * 2
     assert orc.compressed_bytes(64, 64, 1) * 1000 == 625 * 64 * 64
+
+
+# --------------------------------------------------------------------------
+# Prior from a given mask (Table 2) and the convergence diagnostics (Fig. 5)
+# --------------------------------------------------------------------------
+
+def test_prior_from_mask_hand_case_and_invalid_codes(orc):
+    rows = dict((r[0], r[1:]) for r in _golden_rows("metadata_hand_case.txt"))
+    winners = [int(v) for v in rows["winners"]]
+    meta = np.array([[int(rows["meta"][0], 16)]], np.uint32)
+    L = orc.prior_from_mask(meta, 1, 32, 5.0, -1.0)
+    assert (L[0].argmax(1) == winners).all()
+    assert (L[0].max(1) == 5.0).all() and ((L[0] == -1.0).sum(1) == 5).all()
+    # codes that name no candidate (i >= j): every candidate gets `low`
+    meta = np.array([[0x00000000 | (0x5 << 4) | (0xF << 8) | (0x1 << 12)]], np.uint32)
+    L = orc.prior_from_mask(meta, 1, 32, 5.0, -1.0)
+    assert (L[0, :4] == -1.0).all()
+    assert [orc.candidate_of_code(c) for c in (0x4, 0x8, 0xC, 0x9, 0xD, 0xE)] == list(range(6))
+
+
+def test_prior_from_mask_round_trips_hard_compress(orc):
+    rng = np.random.default_rng(21)
+    rows, cols = 9, 96
+    W = rng.integers(0, 1 << 16, (rows, cols), dtype=np.uint64).astype(np.uint16)
+    L = rng.normal(0, 1, (rows, cols // 4, 6)).astype(np.float32)
+    _, meta, idx = orc.hard_compress(W, L)
+    P = orc.prior_from_mask(meta, rows, cols, 3.0, 0.0)
+    assert (P.argmax(2) == idx).all()
+    _, meta2, idx2 = orc.hard_compress(W, P)
+    assert (meta2 == meta).all() and (idx2 == idx).all()
+
+
+def test_mask_stats_large_kappa_freezes_the_samples(orc):
+    """Fig. 5: an inappropriately large kappa suppresses exploration -- the
+    sampled mask is the hard mask at every step and the mask difference
+    between adjacent steps is zero."""
+    rng = np.random.default_rng(22)
+    rows, cols = 16, 256
+    L = rng.normal(0, 1, (rows, cols // 4, 6)).astype(np.float32)
+    hard = np.array([[orc.hard_index(L[r, k]) for k in range(cols // 4)] for r in range(rows)])
+    prev, _, _ = orc.mask_stats(L, rows, cols, 1.0, 1e6, 5, step=0)
+    cur, l1, mp = orc.mask_stats(L, rows, cols, 1.0, 1e6, 5, step=1, prev_idx=prev)
+    assert (prev == hard).all() and (cur == hard).all()
+    assert (l1 == 0).all()
+    assert np.allclose(mp, cols // 4, rtol=1e-9)       # max probability -> 1 per group
+
+
+def test_mask_stats_zero_kappa_is_uniform_random(orc):
+    """kappa = 0: every candidate equally likely at every step (Gumbel-max over
+    equal logits), so the sample is uniform and independent across steps.
+    Two independent uniform candidates differ in L1 by 0 (same, p = 1/6), 2
+    (one shared position, p = 4/6) or 4 (complementary pairs, p = 1/6): the
+    expected distance is exactly 2 per group; the maximum probability is
+    exactly 1/6."""
+    rows, cols = 100, 1600
+    G = rows * cols // 4
+    L = np.random.default_rng(23).normal(0, 1, (rows, cols // 4, 6)).astype(np.float32)
+    prev, _, _ = orc.mask_stats(L, rows, cols, 1.0, 0.0, 9, step=10)
+    cur, l1, mp = orc.mask_stats(L, rows, cols, 1.0, 0.0, 9, step=11, prev_idx=prev)
+    mean = l1.sum() / G
+    assert abs(mean - 2.0) < 5 * math.sqrt(4.0 / 3.0 / G)
+    counts = np.bincount(cur.ravel(), minlength=6)
+    chi2 = ((counts - G / 6) ** 2 / (G / 6)).sum()
+    assert chi2 < 35.0
+    assert np.allclose(mp, (cols // 4) / 6.0, rtol=1e-12)
+
+
+def test_mask_stats_l1_hand_cases(orc):
+    """Force the samples with a large kappa on one-hot logits: candidate 0
+    (0,1) then 5 (2,3) differ in all four positions; 0 then 1 (0,2) in two."""
+    rows, cols = 1, 32
+    def onehot(cands):
+        L = np.full((1, 8, 6), -10.0, np.float32)
+        for k, c in enumerate(cands):
+            L[0, k, c] = 10.0
+        return L
+    a = [0, 0, 1, 2, 3, 4, 5, 2]
+    b = [5, 1, 1, 3, 2, 1, 0, 4]
+    want = [4, 2, 0, 4, 4, 4, 4, 2]   # (0,1)|(2,3) (0,1)|(0,2) same (0,3)|(1,2) ... (1,3)|(0,2) ...
+    prev, _, _ = orc.mask_stats(onehot(a), rows, cols, 1.0, 1e4, 0)
+    cur, l1, _ = orc.mask_stats(onehot(b), rows, cols, 1.0, 1e4, 0, step=1, prev_idx=prev)
+    assert list(prev[0]) == a and list(cur[0]) == b
+    assert l1[0] == sum(want)
+
+
+def test_mask_stats_sample_is_the_forward_argmax(orc):
+    from semi_structured_sparsity_gb300 import workloads as wl
+    W, L, _ = wl.random_case(8, 128, seed=24)
+    Wb, Ln = wl.bf16_bits(W), L.numpy()
+    _, _, probs, _ = orc.forward(Wb, Ln, 0.5, 30.0, 3, 4, 5, want_probs=True)
+    idx, _, _ = orc.mask_stats(Ln, 8, 128, 0.5, 30.0, 3, step=4, tensor_id=5)
+    assert (idx == probs.argmax(2)).all()
