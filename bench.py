@@ -351,6 +351,8 @@ def run_gpu(args):
     if (dominant, shape_key) in tt and tt[(dominant, shape_key)][1] == digest:
         traffic = tt[(dominant, shape_key)][0]
 
+    extras = run_extras(blk, peak, dev)
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, blk, ranks, dev)
@@ -387,6 +389,7 @@ def run_gpu(args):
                      / blk.launches_per_call,
                      "launches_per_step": blk.launches_per_call},
         "kernel_variant": args.kernels,
+        "extras": extras,
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,
@@ -395,6 +398,56 @@ def run_gpu(args):
     if ranks.rank == 0:
         print(json.dumps(line), flush=True)
     ranks.close()
+
+
+def run_extras(blk, peak, dev, reps=20):
+    """The entry points beyond the step, on the same resident block: logits
+    from a given mask (6.125 B/weight: codes in, logits out) and the
+    convergence diagnostics (6.5 B/weight: logits and previous draws in,
+    draws out), each over all matrices, CUDA-event timed."""
+    import torch
+    mk, wl = blk.mk, blk.wl
+    L = mk.lib()
+    s = torch.cuda.current_stream(dev).cuda_stream
+    draws = [torch.zeros((m["x"].rows, m["x"].cols // 4), dtype=torch.uint8, device=dev)
+             for m in blk.mats]
+    nxt = [torch.empty_like(d) for d in draws]
+    l1 = [torch.empty((m["x"].rows,), dtype=torch.int32, device=dev) for m in blk.mats]
+    mp = [torch.empty((m["x"].rows,), dtype=torch.float32, device=dev) for m in blk.mats]
+
+    def prior_from_mask():
+        for m in blk.mats:
+            st = L.maskllm_prior_from_mask(m["meta_out"].data_ptr(), m["x"].rows, m["x"].cols,
+                                           1.0, 0.0, m["logits_out"].data_ptr(), s)
+            assert st == 0
+
+    def mask_stats(step):
+        for i, m in enumerate(blk.mats):
+            st = L.maskllm_mask_stats(m["logits"].data_ptr(), draws[i].data_ptr(), m["x"].rows,
+                                      m["x"].cols, wl.tau, wl.kappa,
+                                      mk.maskllm_rng(0, step, m["tensor_id"]), nxt[i].data_ptr(),
+                                      l1[i].data_ptr(), mp[i].data_ptr(), s)
+            assert st == 0
+
+    out = {}
+    for name, fn, bpw in (("prior_from_mask", lambda i: prior_from_mask(), 6.125),
+                          ("mask_stats", mask_stats, 6.5)):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(reps):
+            fn(i)
+        b.record()
+        torch.cuda.synchronize(dev)
+        sec = a.elapsed_time(b) / 1e3 / reps
+        gbs = bpw * blk.weights / sec / 1e9
+        out[name] = {"us_per_block": round(sec * 1e6, 2), "GB_per_s": round(gbs, 1),
+                     "frac_of_hbm": round(gbs / peak, 4), "bytes_per_weight": bpw,
+                     "launches_per_block": len(blk.mats)}
+    return out
 
 
 def run_e2e(args, blk, ranks, dev):

@@ -161,6 +161,45 @@ maskllm_status maskllm_decompress(const uint16_t* values, const uint32_t* meta, 
 maskllm_status maskllm_noise_words(maskllm_rng rng, int64_t group_begin, int64_t n,
                                    uint32_t* out4, maskllm_stream_t stream);
 
+/* Logits that start from a given mask (MaskLLM Table 2: learned masks are
+ * initialised from a prior mask and refined; masks transfer across tasks).
+ * For every group, logits_out = high on the candidate its 4-bit code names
+ * and low on the other five; a code that names no candidate (anything but
+ * 0x4 0x8 0xC 0x9 0xD 0xE) gives low on all six.
+ *   meta        in   uint32 [rows, cols/32], the layout maskllm_hard_compress writes
+ *   high, low   in   finite
+ *   logits_out  out  fp32 [rows, cols/4, 6]
+ * Moves 6.125 bytes per weight. */
+maskllm_status maskllm_prior_from_mask(const uint32_t* meta, int64_t rows, int64_t cols,
+                                       float high, float low, float* logits_out,
+                                       maskllm_stream_t stream);
+
+/* Convergence diagnostics of one step (MaskLLM Fig. 5: (a) the L1 distance of
+ * sampled masks between adjacent training steps, (b) the maximum probability
+ * of the mask distribution, both governed by kappa).
+ *   draw        the candidate sampled for each group at this step: the first
+ *               maximum of z (see the notation above) -- the candidate the
+ *               soft mask of maskllm_forward tends to as tau -> 0
+ *   l1          per row, sum over groups of the L1 distance (0, 2 or 4)
+ *               between this step's drawn mask and the mask of prev_idx
+ *   maxprob     per row, sum over groups of max_c softmax(fl32(kappa * L))_c,
+ *               the categorical distribution the draw samples from (divide by
+ *               cols/4 for the row mean)
+ *   logits          in   fp32 [rows, cols/4, 6]
+ *   prev_idx        in   uint8 [rows, cols/4], the previous step's draws
+ *                        (entries 0..5), or NULL when there is none
+ *   tau, kappa, rng in   as for maskllm_forward (same noise as the forward of
+ *                        this step)
+ *   idx_out         out  uint8 [rows, cols/4] = the draws, or NULL
+ *   l1_row_out      out  uint32 [rows], or NULL; requires prev_idx
+ *   maxprob_row_out out  fp32 [rows], or NULL
+ * cols <= 2^24 (the per-row L1 is summed exactly in fp32).  Moves 6.25-6.5
+ * bytes per weight. */
+maskllm_status maskllm_mask_stats(const float* logits, const uint8_t* prev_idx, int64_t rows,
+                                  int64_t cols, float tau, float kappa, maskllm_rng rng,
+                                  uint8_t* idx_out, uint32_t* l1_row_out,
+                                  float* maxprob_row_out, maskllm_stream_t stream);
+
 /* ---- Batched calls ------------------------------------------------------
  * One launch processes up to MASKLLM_MAX_BATCH matrices (for example the
  * seven linears of a transformer block); longer lists are split into several

@@ -25,7 +25,8 @@ STATUS = {0: "MASKLLM_OK", 1: "MASKLLM_ERR_INVALID_ARG", 2: "MASKLLM_ERR_SHAPE",
 EXPORTS = ("maskllm_prior_init", "maskllm_forward", "maskllm_backward",
            "maskllm_hard_compress", "maskllm_decompress", "maskllm_noise_words",
            "maskllm_prior_init_batched", "maskllm_forward_batched", "maskllm_backward_batched",
-           "maskllm_hard_compress_batched", "maskllm_set_wait_timeout",
+           "maskllm_hard_compress_batched", "maskllm_prior_from_mask", "maskllm_mask_stats",
+           "maskllm_set_wait_timeout",
            "maskllm_test_withhold_loads", "maskllm_device_status", "maskllm_status_string",
            "maskllm_last_cuda_error")
 MAX_BATCH = 16
@@ -75,6 +76,8 @@ def lib() -> C.CDLL:
         L.maskllm_forward_batched.argtypes = [mp, i32, f32, f32, u64, u32, vp]
         L.maskllm_backward_batched.argtypes = [mp, i32, f32, f32, u64, u32, f32, vp]
         L.maskllm_hard_compress_batched.argtypes = [mp, i32, vp]
+        L.maskllm_prior_from_mask.argtypes = [vp, i64, i64, f32, f32, vp, vp]
+        L.maskllm_mask_stats.argtypes = [vp, vp, i64, i64, f32, f32, maskllm_rng, vp, vp, vp, vp]
         L.maskllm_set_wait_timeout.argtypes = [u64]
         L.maskllm_test_withhold_loads.argtypes = [i32]
         for fn in EXPORTS[:-2]:
@@ -273,3 +276,34 @@ def maskllm_set_wait_timeout(nanoseconds: int) -> None:
 
 def maskllm_test_withhold_loads(enable: bool) -> None:
     _check("maskllm_test_withhold_loads", lib().maskllm_test_withhold_loads(int(bool(enable))))
+
+
+def maskllm_prior_from_mask(meta, rows, cols, high, low, logits_out=None, stream=None):
+    _need(meta, "meta", torch.int32, (rows, cols // 32))
+    logits_out = _out(logits_out, "logits_out", torch.float32, (rows, cols // 4, 6), meta)
+    _check("maskllm_prior_from_mask", lib().maskllm_prior_from_mask(
+        _ptr(meta), rows, cols, high, low, _ptr(logits_out), _stream(stream)))
+    return logits_out
+
+
+def maskllm_mask_stats(logits, tau, kappa, rng, prev_idx=None, idx_out=None, want_idx=True,
+                       want_l1=None, want_maxprob=True, stream=None):
+    """Returns (idx u8 [rows, cols/4] | None, l1 int32 [rows] | None, maxprob f32 [rows] | None).
+    The L1 row sums are uint32 values carried in an int32 tensor."""
+    rows, g, six = logits.shape
+    cols = 4 * g
+    _need(logits, "logits", torch.float32, (rows, g, 6))
+    if prev_idx is not None:
+        _need(prev_idx, "prev_idx", torch.uint8, (rows, g))
+    if idx_out is None and want_idx:
+        idx_out = torch.empty((rows, g), dtype=torch.uint8, device=logits.device)
+    elif idx_out is not None:
+        _need(idx_out, "idx_out", torch.uint8, (rows, g))
+    if want_l1 is None:
+        want_l1 = prev_idx is not None
+    l1 = torch.empty((rows,), dtype=torch.int32, device=logits.device) if want_l1 else None
+    mp = torch.empty((rows,), dtype=torch.float32, device=logits.device) if want_maxprob else None
+    _check("maskllm_mask_stats", lib().maskllm_mask_stats(
+        _ptr(logits), _ptr(prev_idx), rows, cols, tau, kappa, _rng(rng), _ptr(idx_out), _ptr(l1),
+        _ptr(mp), _stream(stream)))
+    return idx_out, l1, mp

@@ -63,6 +63,13 @@ cudaError_t stream_forward(const Device& d, const StreamMatrix* m, int n, float 
 cudaError_t stream_backward(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
                             RngArgs rng, float reg_coeff, cudaStream_t s);
 cudaError_t stream_hard_compress(const Device& d, const StreamMatrix* m, int n, cudaStream_t s);
+// G = previous draws (u8 per group, nullable); out0 = draws (nullable);
+// out1 = L1 distance per row (u32, needs G); out2 = max-probability sum per row
+cudaError_t stream_mask_stats(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
+                              RngArgs rng, cudaStream_t s);
+cudaError_t launch_prior_from_mask(const Device& d, const uint32_t* meta, int64_t rows,
+                                   int64_t cols, float high, float low, float* logits,
+                                   cudaStream_t s);
 void stream_set_wait_ns(uint64_t ns);
 uint64_t stream_wait_ns();
 void stream_set_withhold_loads(int on);

@@ -119,6 +119,53 @@ __global__ void __launch_bounds__(256) decompress_kernel(const uint4* __restrict
   }
 }
 
+// Logits from a given mask ("MaskLLM" project page, Table 2: learned masks
+// start from a prior mask): high on the candidate a group's 4-bit code names,
+// low on the other five; a code naming no candidate gives low everywhere.
+// Candidate of each code, one nibble per code (0xF = none):
+// 0x4 -> c0, 0x8 -> c1, 0xC -> c2, 0x9 -> c3, 0xD -> c4, 0xE -> c5.
+constexpr uint64_t kCandOfCode = 0xF542FF31FFF0FFFFull;
+constexpr int kPfmThreads = 256;
+
+// A warp covers 64 groups (32 threads x 2): each thread reads the metadata
+// byte of its two groups, writes its 48 bytes of logits into a warp-private
+// shared buffer, and the warp then stores the buffer with 16-byte stores that
+// are contiguous across lanes.
+__global__ void __launch_bounds__(kPfmThreads) prior_from_mask_kernel(
+    const uint8_t* __restrict__ meta_bytes, float4* __restrict__ L, int64_t items, float high,
+    float low) {
+  __shared__ __align__(16) float4 buf[kPfmThreads / 32][96];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (kPfmThreads / 32);
+  for (int64_t tile = blockIdx.x * (int64_t)(kPfmThreads / 32) + warp; tile * 32 < items;
+       tile += warps_total) {
+    const int64_t item = tile * 32 + lane;          // two groups: 2*item, 2*item + 1
+    const int64_t left = items - tile * 32;         // items in this tile (<= 32 used)
+    const int n_items = static_cast<int>(left < 32 ? left : 32);
+    if (lane < n_items) {
+      const uint32_t b = __ldcs(meta_bytes + item);
+      float v[12];
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const uint32_t cand = static_cast<uint32_t>(kCandOfCode >> (4 * ((b >> (4 * g)) & 0xFu))) & 0xFu;
+#pragma unroll
+        for (int c = 0; c < kCand; ++c) v[6 * g + c] = (static_cast<uint32_t>(c) == cand) ? high : low;
+      }
+      buf[warp][3 * lane + 0] = make_float4(v[0], v[1], v[2], v[3]);
+      buf[warp][3 * lane + 1] = make_float4(v[4], v[5], v[6], v[7]);
+      buf[warp][3 * lane + 2] = make_float4(v[8], v[9], v[10], v[11]);
+    }
+    __syncwarp();
+    float4* dst = L + 3 * tile * 32;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int q = lane + 32 * k;                    // 16-byte chunk of the tile
+      if (q < 3 * n_items) __stcs(dst + q, buf[warp][q]);
+    }
+    __syncwarp();
+  }
+}
+
 struct NoiseParams {
   uint4* out;
   int64_t group_begin;
@@ -158,6 +205,18 @@ cudaError_t launch_decompress(const Device& d, const uint16_t* values, const uin
   const int64_t items = rows * cols / 32;
   decompress_kernel<<<grid_for(items, 256, d, 8), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(values), meta, reinterpret_cast<uint4*>(W_out), items);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prior_from_mask(const Device& d, const uint32_t* meta, int64_t rows,
+                                   int64_t cols, float high, float low, float* logits,
+                                   cudaStream_t s) {
+  const int64_t items = rows * cols / 8;   // pairs of groups = metadata bytes
+  const int64_t tiles = (items + 31) / 32;
+  const int64_t want = (tiles + kPfmThreads / 32 - 1) / (kPfmThreads / 32);
+  const int64_t cap = 8LL * d.num_sms;
+  prior_from_mask_kernel<<<static_cast<int>(want < cap ? want : cap), kPfmThreads, 0, s>>>(
+      reinterpret_cast<const uint8_t*>(meta), reinterpret_cast<float4*>(logits), items, high, low);
   return cudaGetLastError();
 }
 

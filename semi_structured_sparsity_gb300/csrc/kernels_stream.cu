@@ -239,7 +239,9 @@ __device__ __forceinline__ void store_w_global(void* out, int64_t t, const uint3
 // ---------------------------------------------------------------------------
 // Per-op policies (GPT = groups per consumer thread).
 //   kTable      the Gumbel table is loaded into shared memory
-//   kRowSq      consumers leave per-thread row partials for the producer
+//   kRowQuantities  per-row sums the consumers leave as per-thread partials
+//               (at kPartOffset + t * kPartStride + 4 q of the stage) for the
+//               producer to reduce and hand to write_row()
 //   kStaged     consumers write the chunk's output into the stage; the
 //               producer bulk-stores it (kOutBytesPerGroup bytes per group
 //               from stage offset kOutOffset to out0)
@@ -253,13 +255,17 @@ struct OpBase {
   static constexpr int kConsumerWarps = kConsumers / 32;
   static constexpr int kThreads = kConsumers + 32;   // + the producer warp
   static constexpr int kStages = kStages_;
-  // a thread's row partial is left in its own (already read) W slot
-  static constexpr uint32_t kPartStride = 8 * GPT_;
+  // per-row sums: none by default (see FwdOp, StatsOp)
+  static constexpr int kRowQuantities = 0;
+  static constexpr uint32_t kPartOffset = 0;
+  static constexpr uint32_t kPartStride = 0;
+  __device__ static bool want_row(const MatDesc&, int) { return false; }
+  __device__ static void write_row(const MatDesc&, int64_t, int, float) {}
 };
 
 template <int GPT>
 struct PriorOp : OpBase<GPT, 4> {
-  static constexpr bool kTable = false, kRowSq = false, kStaged = true, kWarpWide = false;
+  static constexpr bool kTable = false, kStaged = true, kWarpWide = false;
   static constexpr bool kOutOverlapsInput = false;   // W in, logits out: separate regions
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
   static constexpr uint32_t kOutOffset = kChunkGroups * 8;
@@ -272,7 +278,7 @@ struct PriorOp : OpBase<GPT, 4> {
   }
 
   __device__ static void consume(const StreamParams& p, const MatDesc&, const Chunk&, uint8_t* st,
-                                 int t, const float*, float&) {
+                                 int t, const float*, float*) {
     uint32_t w[2 * GPT];
     load_w<GPT>(st, t, w);
     float out[6 * GPT];
@@ -295,8 +301,17 @@ struct PriorOp : OpBase<GPT, 4> {
 
 template <bool kProbs, int GPT>
 struct FwdOp : OpBase<GPT, 4> {
-  static constexpr bool kTable = true, kRowSq = true, kStaged = false, kWarpWide = false;
+  static constexpr bool kTable = true, kStaged = false, kWarpWide = false;
   static constexpr bool kOutOverlapsInput = false;
+  // row sum of squares; a thread's partial is left in its own, already
+  // consumed, W slot of the stage
+  static constexpr int kRowQuantities = 1;
+  static constexpr uint32_t kPartOffset = 0;
+  static constexpr uint32_t kPartStride = 8 * GPT;
+  __device__ static bool want_row(const MatDesc& d, int) { return d.out1 != nullptr; }
+  __device__ static void write_row(const MatDesc& d, int64_t row, int, float v) {
+    static_cast<float*>(d.out1)[row] = v;
+  }
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
   static constexpr uint32_t kOutOffset = 0;
   static constexpr uint32_t kOutBytesPerGroup = 0;
@@ -333,7 +348,7 @@ struct FwdOp : OpBase<GPT, 4> {
   }
 
   __device__ static void consume(const StreamParams& p, const MatDesc& d, const Chunk& c,
-                                 uint8_t* st, int t, const float* tab, float& acc) {
+                                 uint8_t* st, int t, const float* tab, float* acc) {
     uint32_t w[2 * GPT], o[2 * GPT];
     float L[6 * GPT], pr[6 * GPT];
     load_w<GPT>(st, t, w);
@@ -342,7 +357,7 @@ struct FwdOp : OpBase<GPT, 4> {
 #pragma unroll
     for (int g = 0; g < GPT; ++g)
       group(p, tab, g0 + g, d.tensor_id, L + 6 * g, w[2 * g], w[2 * g + 1], o[2 * g],
-            o[2 * g + 1], acc, pr + 6 * g);
+            o[2 * g + 1], acc[0], pr + 6 * g);
     const int64_t unit = c.g0 / GPT + t;   // this thread's GPT-group unit
     store_w_global<GPT>(d.out0, unit, o);
     if (kProbs && d.out2 != nullptr) store_l<GPT>(d.out2, unit, pr);
@@ -351,7 +366,7 @@ struct FwdOp : OpBase<GPT, 4> {
 
 template <bool kReg, int GPT>
 struct BwdOp : OpBase<GPT, 4> {
-  static constexpr bool kTable = true, kRowSq = false, kStaged = true, kWarpWide = false;
+  static constexpr bool kTable = true, kStaged = true, kWarpWide = false;
   static constexpr bool kOutOverlapsInput = true;    // dlogits overwrite the logits
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 8 + 24);
   static constexpr uint32_t kOutOffset = kChunkGroups * 16;
@@ -396,7 +411,7 @@ struct BwdOp : OpBase<GPT, 4> {
   }
 
   __device__ static void consume(const StreamParams& p, const MatDesc& d, const Chunk& c,
-                                 uint8_t* st, int t, const float* tab, float&) {
+                                 uint8_t* st, int t, const float* tab, float*) {
     uint32_t w[2 * GPT], gr[2 * GPT];
     float L[6 * GPT], dl[6 * GPT];
     load_w<GPT>(st, t, w);
@@ -438,7 +453,7 @@ __device__ __forceinline__ uint32_t gather_selector(int c) {
 
 template <int GPT>
 struct CompressOp : OpBase<GPT, 4> {
-  static constexpr bool kTable = false, kRowSq = false, kStaged = false, kWarpWide = true;
+  static constexpr bool kTable = false, kStaged = false, kWarpWide = true;
   static constexpr bool kOutOverlapsInput = false;
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
   static constexpr uint32_t kOutOffset = 0;
@@ -449,7 +464,7 @@ struct CompressOp : OpBase<GPT, 4> {
   }
 
   __device__ static void consume(const StreamParams&, const MatDesc& k, const Chunk& c,
-                                 uint8_t* st, int t, const float*, float&) {
+                                 uint8_t* st, int t, const float*, float*) {
     // Every lane comes here.  Chunks hold a multiple of 8 groups, so the
     // 8/GPT lanes that share one 32-bit code word are all active or all not.
     constexpr int kLanesPerWord = 8 / GPT;
@@ -486,6 +501,88 @@ struct CompressOp : OpBase<GPT, 4> {
   }
 };
 
+// Convergence diagnostics ("MaskLLM" project page, Fig. 5): per step, the
+// candidate drawn for every group (the first maximum of the noisy logits z,
+// the mask the soft mask tends to as tau -> 0), the L1 distance of the drawn
+// masks to the previous step's draws, and the maximum probability of the
+// categorical distribution softmax(fl32(kappa * L)) the draw samples from.
+// Candidate c's kept positions as a 4-bit mask (bit j = position j), one
+// nibble per candidate: c0 0011, c1 0101, c2 1001, c3 0110, c4 1010, c5 1100.
+constexpr uint32_t kKeepBits = 0xCA6953u;
+
+template <int GPT>
+struct StatsOp : OpBase<GPT, 4> {
+  static constexpr bool kTable = true, kStaged = false, kWarpWide = false;
+  static constexpr bool kOutOverlapsInput = false;
+  static constexpr uint32_t kOutOffset = 0;
+  static constexpr uint32_t kOutBytesPerGroup = 0;
+  // logits, then two per-thread partials (L1 distance, max probability)
+  static constexpr int kRowQuantities = 2;
+  static constexpr uint32_t kPartOffset = kChunkGroups * 24;
+  static constexpr uint32_t kPartStride = 8;
+  static constexpr uint32_t kStageBytes = kPartOffset + (kChunkGroups / GPT) * kPartStride;
+
+  __device__ static bool want_row(const MatDesc& d, int q) {
+    return q == 0 ? (d.out1 != nullptr && d.G != nullptr) : d.out2 != nullptr;
+  }
+  __device__ static void write_row(const MatDesc& d, int64_t row, int q, float v) {
+    if (q == 0)
+      static_cast<uint32_t*>(d.out1)[row] = static_cast<uint32_t>(v);   // exact below 2^24
+    else
+      static_cast<float*>(d.out2)[row] = v;
+  }
+
+  __device__ static void issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
+    const uint32_t lb = static_cast<uint32_t>(c.ng) * 24;
+    mbar_expect_tx(bar, lb);
+    bulk_load(st, static_cast<const uint8_t*>(d.L) + c.g0 * 24, lb, bar);
+  }
+
+  __device__ static void consume(const StreamParams& p, const MatDesc& d, const Chunk& c,
+                                 uint8_t* st, int t, const float* tab, float* acc) {
+    float L[6 * GPT];
+    load_l<GPT>(st, t, L);
+    const int64_t unit = c.g0 / GPT + t;
+    uint32_t prev = 0;
+    if (d.G != nullptr) {
+      if constexpr (GPT == 2)
+        prev = static_cast<const uint16_t*>(d.G)[unit];
+      else
+        prev = static_cast<const uint8_t*>(d.G)[unit];
+    }
+    uint32_t drawn = 0;
+    const uint64_t g0 = static_cast<uint64_t>(c.g0) + static_cast<uint64_t>(GPT * t);
+#pragma unroll
+    for (int k = 0; k < GPT; ++k) {
+      const float* Lk = L + 6 * k;
+      float g[kCand], z[kCand], y[kCand];
+      gumbel6(group_words(g0 + k, p.s.step, d.tensor_id, p.s.keys), tab, g);
+#pragma unroll
+      for (int c6 = 0; c6 < kCand; ++c6) {
+        y[c6] = __fmul_rn(p.s.kappa, Lk[c6]);
+        z[c6] = __fmul_rn(__fadd_rn(y[c6], g[c6]), p.s.rho);
+      }
+      const int s = first_argmax6(z);
+      drawn |= static_cast<uint32_t>(s) << (8 * k);
+      if (d.G != nullptr) {
+        const uint32_t q = (prev >> (8 * k)) & 7u;   // entries 6, 7 count as empty masks
+        acc[0] += static_cast<float>(__popc(((kKeepBits >> (4 * s)) ^ (kKeepBits >> (4 * q))) & 0xFu));
+      }
+      const float m = fmaxf(fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3])), fmaxf(y[4], y[5]));
+      float sum = 0.f;
+#pragma unroll
+      for (int c6 = 0; c6 < kCand; ++c6) sum += ex2_approx((y[c6] - m) * kLog2e);
+      acc[1] += rcp_approx(sum);   // the largest term is 2^0 = 1
+    }
+    if (d.out0 != nullptr) {
+      if constexpr (GPT == 2)
+        static_cast<uint16_t*>(d.out0)[unit] = static_cast<uint16_t>(drawn);
+      else
+        static_cast<uint8_t*>(d.out0)[unit] = static_cast<uint8_t>(drawn);
+    }
+  }
+};
+
 // ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
@@ -517,23 +614,27 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
     const Chunk c = held[s];
     const MatDesc& d = p.mats[c.mat];
     const uint8_t* st = stages + s * Op::kStageBytes;
-    if (Op::kRowSq && d.out1 != nullptr && c.nrows > 0) {
-      float* row_sq = static_cast<float*>(d.out1);
-      auto part = [&](int k) {
-        return *reinterpret_cast<const float*>(st + k * Op::kPartStride);
-      };
-      if (d.cpr > 0) {
-        float v = 0.f;
-        for (int k = lane; k < Op::kConsumers; k += 32) v += part(k);
-        v = warp_sum(v);
-        if (lane == 0) row_sq[c.row0] = v;
-      } else {
-        const int tpr = d.gpr / Op::kGPT;   // threads per short row
-        for (int r = 0; r < c.nrows; ++r) {
+    if (Op::kRowQuantities > 0 && c.nrows > 0) {
+#pragma unroll
+      for (int q = 0; q < Op::kRowQuantities; ++q) {
+        if (!Op::want_row(d, q)) continue;
+        auto part = [&](int k) {
+          return *reinterpret_cast<const float*>(st + Op::kPartOffset + k * Op::kPartStride +
+                                                 4 * q);
+        };
+        if (d.cpr > 0) {
           float v = 0.f;
-          for (int k = lane; k < tpr; k += 32) v += part(r * tpr + k);
+          for (int k = lane; k < Op::kConsumers; k += 32) v += part(k);
           v = warp_sum(v);
-          if (lane == 0) row_sq[c.row0 + r] = v;
+          if (lane == 0) Op::write_row(d, c.row0, q, v);
+        } else {
+          const int tpr = d.gpr / Op::kGPT;   // threads per short row
+          for (int r = 0; r < c.nrows; ++r) {
+            float v = 0.f;
+            for (int k = lane; k < tpr; k += 32) v += part(r * tpr + k);
+            v = warp_sum(v);
+            if (lane == 0) Op::write_row(d, c.row0 + r, q, v);
+          }
         }
       }
     }
@@ -622,7 +723,7 @@ __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
   it.init(&p, u0, u1);
   Chunk c;
   int64_t n = 0;
-  float acc = 0.f;
+  float acc[2] = {0.f, 0.f};   // per-row quantities of this thread
   while (it.next(c)) {
     const int s = static_cast<int>(n % S);
     const bool got = mbar_wait_bounded(&full[s], static_cast<uint32_t>((n / S) & 1), p.wait_ns,
@@ -637,17 +738,16 @@ __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
       Op::consume(p, d, c, st, t, tab, acc);   // every lane, active or not
     else if (Op::kGPT * t < c.ng)
       Op::consume(p, d, c, st, t, tab, acc);
-    if (Op::kRowSq) {
-      // the row partial goes into this thread's own W slot, already read
-      float* part = reinterpret_cast<float*>(st + t * Op::kPartStride);
-      if (d.cpr > 0) {
-        if (c.nrows > 0) {
-          *part = acc;   // the row ends in this chunk
-          acc = 0.f;
+    if (Op::kRowQuantities > 0) {
+      float* part = reinterpret_cast<float*>(st + Op::kPartOffset + t * Op::kPartStride);
+      if (d.cpr == 0 || c.nrows > 0) {
+        // the row ends in this chunk (long rows), or each thread's groups lie
+        // in one short row of this chunk
+#pragma unroll
+        for (int q = 0; q < Op::kRowQuantities; ++q) {
+          part[q] = acc[q];
+          acc[q] = 0.f;
         }
-      } else {
-        *part = acc;     // short rows: each thread's groups lie in one row
-        acc = 0.f;
       }
     }
     if (Op::kStaged) fence_proxy_async_smem();
@@ -757,6 +857,7 @@ static_assert(Layout<FwdOp<true, kGPT>>::kBytes <= 232448, "forward shared memor
 static_assert(Layout<BwdOp<true, kGPT>>::kBytes <= 232448, "backward shared memory");
 static_assert(Layout<PriorOp<kGPT>>::kBytes <= 232448, "prior shared memory");
 static_assert(Layout<CompressOp<kGPT>>::kBytes <= 232448, "compress shared memory");
+static_assert(Layout<StatsOp<kGPT>>::kBytes <= 232448, "stats shared memory");
 static_assert(sizeof(StreamParams) <= 4000, "kernel parameters");
 
 cudaError_t stream_prior_init(const Device& d, const StreamMatrix* m, int n, float scale,
@@ -789,6 +890,14 @@ cudaError_t stream_hard_compress(const Device& d, const StreamMatrix* m, int n, 
   describe(p, m, n);
   p.s = scalars(1.0f, 0.0f, {0, 0, 0}, 0.0f, 0.0f);
   return launch<CompressOp<kGPT>>(d, p, s);
+}
+
+cudaError_t stream_mask_stats(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
+                              RngArgs rng, cudaStream_t s) {
+  StreamParams p;
+  describe(p, m, n);
+  p.s = scalars(tau, kappa, rng, 0.0f, 0.0f);
+  return launch<StatsOp<kGPT>>(d, p, s);
 }
 
 void stream_set_wait_ns(uint64_t ns) { g_wait_ns = ns; }

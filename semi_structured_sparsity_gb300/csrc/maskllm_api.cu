@@ -446,6 +446,63 @@ maskllm_status maskllm_noise_words(maskllm_rng rng, int64_t group_begin, int64_t
       d, {rng.seed, rng.step, rng.tensor_id}, group_begin, n, out4, stream));
 }
 
+maskllm_status maskllm_prior_from_mask(const uint32_t* meta, int64_t rows, int64_t cols,
+                                       float high, float low, float* logits_out,
+                                       maskllm_stream_t stream) {
+  const void* ptrs[] = {meta, logits_out};
+  MK_TRY(maskllm::check_ptrs(ptrs, 2));
+  MK_TRY(maskllm::check_shape(rows, cols));
+  if (!isfinite(high) || !isfinite(low)) return MASKLLM_ERR_INVALID_ARG;
+  const uint64_t n = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols);
+  maskllm::Spans sp;
+  sp.input(meta, n / 8);
+  sp.output(logits_out, 6 * n);
+  MK_TRY(sp.check());
+  maskllm::Device d;
+  cudaError_t e = maskllm::current_device(&d);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
+  return maskllm::finish(
+      maskllm::launch_prior_from_mask(d, meta, rows, cols, high, low, logits_out, stream));
+}
+
+maskllm_status maskllm_mask_stats(const float* logits, const uint8_t* prev_idx, int64_t rows,
+                                  int64_t cols, float tau, float kappa, maskllm_rng rng,
+                                  uint8_t* idx_out, uint32_t* l1_row_out,
+                                  float* maxprob_row_out, maskllm_stream_t stream) {
+  const void* ptrs[] = {logits};
+  MK_TRY(maskllm::check_ptrs(ptrs, 1));
+  MK_TRY(maskllm::check_optional(prev_idx));
+  MK_TRY(maskllm::check_optional(idx_out));
+  MK_TRY(maskllm::check_optional(l1_row_out));
+  MK_TRY(maskllm::check_optional(maxprob_row_out));
+  if (l1_row_out != nullptr && prev_idx == nullptr) return MASKLLM_ERR_INVALID_ARG;
+  MK_TRY(maskllm::check_shape(rows, cols));
+  if (cols > (int64_t(1) << 24)) return MASKLLM_ERR_SHAPE;
+  MK_TRY(maskllm::check_temperature(tau, kappa));
+  const uint64_t n = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols);
+  maskllm::Spans sp;
+  sp.input(logits, 6 * n);
+  sp.input(prev_idx, n / 4);
+  sp.output(idx_out, n / 4);
+  sp.output(l1_row_out, 4 * static_cast<uint64_t>(rows));
+  sp.output(maxprob_row_out, 4 * static_cast<uint64_t>(rows));
+  MK_TRY(sp.check());
+  maskllm::Device d;
+  cudaError_t e = maskllm::current_device(&d);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
+  maskllm::StreamMatrix m{};
+  m.L = logits;
+  m.G = prev_idx;
+  m.out0 = idx_out;
+  m.out1 = l1_row_out;
+  m.out2 = maxprob_row_out;
+  m.rows = rows;
+  m.cols = cols;
+  m.tensor_id = rng.tensor_id;
+  return maskllm::finish(maskllm::stream_mask_stats(d, &m, 1, tau, kappa,
+                                                    {rng.seed, rng.step, rng.tensor_id}, stream));
+}
+
 maskllm_status maskllm_set_wait_timeout(uint64_t nanoseconds) {
   maskllm::stream_set_wait_ns(nanoseconds);
   return MASKLLM_OK;

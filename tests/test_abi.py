@@ -146,3 +146,15 @@ def test_batched_alias_across_launches(L):
         arr[i] = _mat(W=off, logits_out=off + 0x10000)
     arr[19].logits_out = base + 0x10        # writes over matrix 0's W, in another launch
     assert L.maskllm_prior_init_batched(arr, n, 1.0, None) == ALIAS
+
+
+def test_next_entry_points_validation(L):
+    r = _rng()
+    assert L.maskllm_prior_from_mask(A, 4, 64, float("inf"), 0.0, B, None) == INVALID
+    assert L.maskllm_prior_from_mask(A, 4, 48, 1.0, 0.0, B, None) == SHAPE
+    assert L.maskllm_prior_from_mask(A, 4, 64, 1.0, 0.0, A + 16, None) == ALIAS
+    # the L1 distance needs the previous draws; cols above 2^24; tau <= 0
+    assert L.maskllm_mask_stats(A, None, 4, 64, 1.0, 1.0, r, None, B, None, None) == INVALID
+    assert L.maskllm_mask_stats(A, None, 1, (1 << 24) + 32, 1.0, 1.0, r, None, None, Cc, None) == SHAPE
+    assert L.maskllm_mask_stats(A, None, 4, 64, 0.0, 1.0, r, None, None, Cc, None) == INVALID
+    assert L.maskllm_mask_stats(A, None, 4, 64, 1.0, 1.0, r, A + 64, None, None, None) == ALIAS

@@ -1,0 +1,86 @@
+"""GPU parity of the entry points beyond the training step: logits from a
+given mask (MaskLLM Table 2) and the convergence diagnostics (MaskLLM Fig. 5),
+against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from semi_structured_sparsity_gb300 import binding as mk
+from semi_structured_sparsity_gb300 import workloads as wl
+from tests._helpers import assert_bits_equal, assert_close, bits32
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(1, 32), (3, 96), (7, 160), (300, 64), (5, 4128), (33, 11008), (256, 1024)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mk.lib()
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES)
+def test_prior_from_mask_bit_exact(rows, cols):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(rows * 11 + cols)
+    meta = torch.randint(-2**31, 2**31 - 1, (rows, cols // 32), generator=gen, device="cuda",
+                         dtype=torch.int64).to(torch.int32)   # every code, valid or not
+    L = mk.maskllm_prior_from_mask(meta, rows, cols, 7.5, -0.25)
+    torch.cuda.synchronize()
+    want = orc.prior_from_mask(bits32(meta), rows, cols, 7.5, -0.25)
+    assert_bits_equal(bits32(L), want.view(np.uint32), "logits from mask")
+
+
+def test_prior_from_mask_round_trips_hard_compress():
+    W, L, _ = wl.random_case(64, 4096, seed=77, device="cuda")
+    vals, meta, idx = mk.maskllm_hard_compress(W, L, want_idx=True)
+    P = mk.maskllm_prior_from_mask(meta, 64, 4096, 1.0, 0.0)
+    vals2, meta2, idx2 = mk.maskllm_hard_compress(W, P, want_idx=True)
+    torch.cuda.synchronize()
+    assert torch.equal(meta, meta2) and torch.equal(idx, idx2) and torch.equal(vals, vals2)
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES)
+@pytest.mark.parametrize("tau,kappa", [(1.0, 3.0), (0.2, 500.0), (4.0, 0.0), (0.5, 1e6)])
+def test_mask_stats_match_oracle(rows, cols, tau, kappa):
+    _, L, _ = wl.random_case(rows, cols, seed=rows + cols, device="cuda")
+    rng_prev, rng = (5, 10, 3), (5, 11, 3)
+    prev, _, _ = mk.maskllm_mask_stats(L, tau, kappa, rng_prev)
+    idx, l1, mp = mk.maskllm_mask_stats(L, tau, kappa, rng, prev_idx=prev)
+    none_idx, none_l1, none_mp = mk.maskllm_mask_stats(L, tau, kappa, rng, want_idx=False)
+    torch.cuda.synchronize()
+    Lh = L.cpu().numpy()
+    wprev, _, _ = orc.mask_stats(Lh, rows, cols, tau, kappa, *rng_prev)
+    widx, wl1, wmp = orc.mask_stats(Lh, rows, cols, tau, kappa, *rng, prev_idx=wprev)
+    assert_bits_equal(prev.cpu().numpy(), wprev, "previous draws")
+    assert_bits_equal(idx.cpu().numpy(), widx, "draws")
+    assert_bits_equal(l1.cpu().numpy().view(np.uint32), wl1.astype(np.uint32), "L1 per row")
+    assert_close(mp.cpu().numpy(), wmp, rtol=1e-5, atol=0, what="max-probability row sum")
+    assert none_idx is None and none_l1 is None
+    assert torch.equal(none_mp, mp)
+
+
+def test_mask_stats_draw_is_the_forward_argmax():
+    """The draw is the candidate the soft mask of the same step tends to: the
+    first maximum of p as the forward reports it."""
+    W, L, _ = wl.random_case(64, 2048, seed=91, device="cuda")
+    probs = torch.empty_like(L)
+    mk.maskllm_forward(W, L, 0.5, 30.0, (2, 4, 6), probs_out=probs)
+    idx, _, _ = mk.maskllm_mask_stats(L, 0.5, 30.0, (2, 4, 6))
+    torch.cuda.synchronize()
+    p = probs.cpu().numpy()
+    top = np.sort(p, axis=2)
+    clear = (top[..., -1] - top[..., -2]) > 1e-6      # no near-tie in p
+    assert clear.mean() > 0.99
+    assert (idx.cpu().numpy()[clear] == p.argmax(2)[clear]).all()
+
+
+def test_mask_stats_validation():
+    _, L, _ = wl.random_case(4, 64, seed=1, device="cuda")
+    l1 = torch.empty((4,), dtype=torch.int32, device="cuda")
+    st = mk.lib().maskllm_mask_stats(L.data_ptr(), None, 4, 64, 1.0, 1.0, mk._rng((0, 0, 0)),
+                                     None, l1.data_ptr(), None, None)
+    assert st == 1   # the L1 distance needs the previous draws
