@@ -209,11 +209,16 @@ def traffic_table():
     return out
 
 
+# the sources compiled into the timed stream kernels; a stored traffic
+# figure is valid only for the digest it was taken with
+STREAM_SOURCES = ("device_common.cuh", "kernels_stream.cu", "pipeline.cuh")
+
+
 def kernel_source_digest() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "semi_structured_sparsity_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in STREAM_SOURCES:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:12]
