@@ -86,6 +86,20 @@ def lib():
         L.orc_prior_from_mask.restype = None
         L.orc_mask_stats.argtypes = [f32p, i64, i64, i64, f32, f32, u64, u32, u32, vp, vp, vp, vp]
         L.orc_mask_stats.restype = None
+        i32p = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
+        i32 = C.c_int32
+        L.orc_perm_shift.argtypes = [u16p, i64, i64]
+        L.orc_perm_shift.restype = i32
+        L.orc_perm_fixed.argtypes = [C.c_uint16, i32]
+        L.orc_perm_fixed.restype = u32
+        L.orc_perm_metric_fixed.argtypes = [u16p, i64, i64, i32p, i32]
+        L.orc_perm_metric_fixed.restype = u64
+        L.orc_perm_metric.argtypes = [u16p, i64, i64, i32p]
+        L.orc_perm_metric.restype = C.c_double
+        L.orc_perm_swap_gain.argtypes = [u16p, i64, i64, i32p, i32, i64, i64]
+        L.orc_perm_swap_gain.restype = i64
+        L.orc_perm_search.argtypes = [u16p, i64, i64, i32p, i32, i32, vp, vp]
+        L.orc_perm_search.restype = i32
         _ = (u8p, i64p)
         _lib = L
     return _lib
@@ -254,3 +268,57 @@ def mask_stats(L, rows, cols, tau, kappa, seed, step=0, tensor_id=0, prev_idx=No
     lib().orc_mask_stats(L, rows, cols, row_begin, tau, kappa, seed, step, tensor_id, _ptr(prev),
                          _ptr(idx), _ptr(l1), _ptr(mp))
     return idx, l1, mp
+
+
+# ---------------------------------------------------------------------------
+# channel permutation before pruning
+# ---------------------------------------------------------------------------
+
+PERM_NONFINITE = -(2 ** 31)   # orc_perm_shift's answer for a non-finite weight
+
+
+def perm_shift(W) -> int:
+    W = _c(W, np.uint16)
+    return int(lib().orc_perm_shift(W, W.shape[0], W.shape[1]))
+
+
+def perm_fixed(w_bits: int, shift: int) -> int:
+    return int(lib().orc_perm_fixed(int(w_bits), int(shift)))
+
+
+def perm_metric_fixed(W, perm, shift: int) -> int:
+    W = _c(W, np.uint16)
+    return int(lib().orc_perm_metric_fixed(W, W.shape[0], W.shape[1], _c(perm, np.int32), shift))
+
+
+def perm_metric(W, perm) -> float:
+    W = _c(W, np.uint16)
+    return float(lib().orc_perm_metric(W, W.shape[0], W.shape[1], _c(perm, np.int32)))
+
+
+def perm_swap_gain(W, perm, shift: int, a: int, b: int) -> int:
+    W = _c(W, np.uint16)
+    p = np.array(perm, np.int32)
+    return int(lib().orc_perm_swap_gain(W, W.shape[0], W.shape[1], p, shift, a, b))
+
+
+def perm_swap_gains(W, perm, shift: int):
+    """[cols, cols] int64: the fixed-point gain of every swap (0 within a group)."""
+    W = _c(W, np.uint16)
+    cols = W.shape[1]
+    out = np.zeros((cols, cols), np.int64)
+    for a in range(cols):
+        for b in range(a + 1, cols):
+            out[a, b] = out[b, a] = perm_swap_gain(W, perm, shift, a, b)
+    return out
+
+
+def perm_search(W, perm, shift: int, max_swaps: int):
+    """Returns (perm after the search, swaps int32 [n, 2], gains int64 [n])."""
+    W = _c(W, np.uint16)
+    p = np.array(perm, np.int32)
+    swaps = np.zeros((max(max_swaps, 1), 2), np.int32)
+    gains = np.zeros(max(max_swaps, 1), np.int64)
+    n = int(lib().orc_perm_search(W, W.shape[0], W.shape[1], p, shift, max_swaps, _ptr(swaps),
+                                  _ptr(gains)))
+    return p, swaps[:n].copy(), gains[:n].copy()

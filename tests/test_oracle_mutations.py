@@ -55,6 +55,15 @@ MUTATIONS = {
                  "for (int j = 0; j < 4; ++j) l1 += orc_candidate_keeps(s, j) != orc_candidate_keeps(s, j);"),
     "stats_maxprob_kappa": ("        float a = kappa * L[c];\n        y[c] = (double)a;",
                             "        float a = L[c];\n        y[c] = (double)a;"),
+    "perm_top2": ("  return v[0] + v[1];\n}", "  return v[0] + v[2];\n}"),
+    "perm_metric_abs": ("a[j] = fabs(orc_bf16_to_double(W[r * cols + perm[4 * g + j]]));",
+                        "a[j] = orc_bf16_to_double(W[r * cols + perm[4 * g + j]]);"),
+    "perm_shift_bits": ("return 31 - lr - orc_floor_log2(mx);", "return 32 - lr - orc_floor_log2(mx);"),
+    "perm_fixed_round": ("return (uint32_t)floor(ldexp(", "return (uint32_t)nearbyint(ldexp("),
+    "perm_tie_rule": ("        if (g > best) {", "        if (g >= best && g > 0) {"),
+    "perm_gain_sign": ("  return after - before;", "  return before - after;"),
+    "perm_swap_restore": ("  perm[b] = perm[a];\n  perm[a] = t;\n  return after",
+                          "  perm[a] = t;\n  return after"),
 }
 
 
@@ -74,7 +83,7 @@ def _run_mutant(tmp_root, name, old, new):
     for fn in ("__init__.py", "workloads.py"):
         shutil.copy(os.path.join(ROOT, pkg, fn), os.path.join(d, pkg, fn))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        "tests/test_oracle_pins.py"], cwd=d, capture_output=True, text=True,
+                        "tests/test_oracle_pins.py", "tests/test_oracle_perm_pins.py"], cwd=d, capture_output=True, text=True,
                        timeout=600)
     return name, r.returncode, (r.stdout.strip().splitlines() or [""])[-1]
 
