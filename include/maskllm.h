@@ -200,6 +200,83 @@ maskllm_status maskllm_mask_stats(const float* logits, const uint8_t* prev_idx, 
                                   uint8_t* idx_out, uint32_t* l1_row_out,
                                   float* maxprob_row_out, maskllm_stream_t stream);
 
+/* ---- Channel permutation before pruning ---------------------------------
+ * "Accelerating Sparse Deep Neural Networks", Sec. 4.1 (Fig. 5): permuting
+ * the input channels (columns) of W before 2:4 magnitude pruning raises the
+ * magnitude that pruning keeps; the layer producing those channels permutes
+ * its output rows alike, so the network computes the same function.
+ * "Channel Permutations for N:M Sparsity" (abstract): a quality metric judges
+ * permutations and a search finds good ones.
+ *
+ *   perm      int32 [cols], a permutation of 0..cols-1: slot i of the
+ *             permuted matrix holds channel perm[i], W_perm[r, i] =
+ *             W[r, perm[i]].
+ *   q(w)      = floor(|w| * 2^shift), shift = 31 - ceil(log2 rows) -
+ *             floor(log2 max|w|) (0 for an all-zero W): fixed-point
+ *             magnitudes whose sum over any column is below 2^32.
+ *   metric    = sum over rows and groups of W_perm of the two largest q of
+ *             the group (the magnitude 2:4 magnitude pruning keeps, exact).
+ *   gain(a,b) = metric after exchanging the channels of slots a and b minus
+ *             the metric before; 0 for two slots of one group.
+ *   search    = steepest ascent: apply the swap of largest gain (ties: the
+ *             smallest a, then the smallest b, a < b) while some gain is
+ *             positive, at most max_swaps times.  (The pages mention further
+ *             devices for leaving local optima without describing them; they
+ *             are not implemented.)
+ * All comparisons are on exact integers, so results do not depend on the
+ * order of any addition.  Shapes: the rules above, plus cols <= 32768 and
+ * rows <= 2^24. */
+
+/* shift_out (device int32 [1]) = the fixed-point shift of W, or INT32_MIN
+ * when W holds an infinity or NaN. */
+maskllm_status maskllm_perm_shift(const uint16_t* W, int64_t rows, int64_t cols,
+                                  int32_t* shift_out, maskllm_stream_t stream);
+
+/* metric_out (device uint64 [1]) = the fixed-point metric of perm, with the
+ * shift read from the device int32 *shift (normally maskllm_perm_shift's
+ * output).  An entry of perm outside [0, cols) reads as a zero weight and
+ * makes the next maskllm_device_status() return MASKLLM_ERR_INVALID_ARG. */
+maskllm_status maskllm_perm_metric(const uint16_t* W, int64_t rows, int64_t cols,
+                                   const int32_t* perm, const int32_t* shift,
+                                   uint64_t* metric_out, maskllm_stream_t stream);
+
+/* W_out[r, i] = W[r, perm[i]] (bf16 [rows, cols]); out-of-range entries as for
+ * maskllm_perm_metric (the element is written as +0). */
+maskllm_status maskllm_permute_columns(const uint16_t* W, int64_t rows, int64_t cols,
+                                       const int32_t* perm, uint16_t* W_out,
+                                       maskllm_stream_t stream);
+
+/* Device scratch the two calls below need, in bytes (0 for a shape outside
+ * the rules): a [cols, cols] and two [rows, cols] uint32 tables and a few
+ * hundred bytes of control.  The caller owns it; it holds nothing between
+ * calls. */
+int64_t maskllm_perm_workspace_bytes(int64_t rows, int64_t cols);
+
+/* gains_out (device int64 [cols, cols], symmetric) = gain(a, b) of every pair
+ * of slots under perm.  info_out (device int32 [1]) = 0, or -1 when perm is
+ * not a permutation of 0..cols-1, or -2 when W holds an infinity or NaN (then
+ * gains_out is not written).  shift_out (device int32 [1], nullable) = the
+ * shift used. */
+maskllm_status maskllm_perm_swap_gains(const uint16_t* W, int64_t rows, int64_t cols,
+                                       const int32_t* perm, void* workspace,
+                                       int64_t workspace_bytes, int64_t* gains_out,
+                                       int32_t* info_out, int32_t* shift_out,
+                                       maskllm_stream_t stream);
+
+/* The search, from the permutation in perm (device int32 [cols], updated in
+ * place).  Swap s is logged in swaps_out[2s], swaps_out[2s+1] (the slots a <
+ * b; device int32 [max_swaps, 2], nullable) and gains_out[s] (device int64
+ * [max_swaps], nullable).  n_swaps_out (device int32 [1]) = the number of
+ * swaps applied, or -1 / -2 as info_out above (then perm is unchanged).
+ * shift_out as above.  max_swaps >= 0 steps are enqueued without any
+ * synchronisation; once no swap gains, the remaining steps return at once
+ * (a few microseconds each). */
+maskllm_status maskllm_perm_search(const uint16_t* W, int64_t rows, int64_t cols, int32_t* perm,
+                                   int32_t max_swaps, void* workspace, int64_t workspace_bytes,
+                                   int32_t* swaps_out, int64_t* gains_out,
+                                   int32_t* n_swaps_out, int32_t* shift_out,
+                                   maskllm_stream_t stream);
+
 /* ---- Batched calls ------------------------------------------------------
  * One launch processes up to MASKLLM_MAX_BATCH matrices (for example the
  * seven linears of a transformer block); longer lists are split into several
@@ -255,9 +332,10 @@ maskllm_status maskllm_set_wait_timeout(uint64_t nanoseconds);
  * launches issued while enabled are invalid.  Host-global setting. */
 maskllm_status maskllm_test_withhold_loads(int32_t enable);
 
-/* Waits for `stream`, then reads and clears the library's device error word
+/* Waits for `stream`, then reads and clears the library's device error words
  * on the current device.  Returns MASKLLM_ERR_TIMEOUT if a bounded wait inside
  * a kernel gave up since the last call (its results are then invalid),
+ * else MASKLLM_ERR_INVALID_ARG if a permutation entry was out of range,
  * MASKLLM_ERR_CUDA if the wait itself failed, MASKLLM_OK otherwise. */
 maskllm_status maskllm_device_status(maskllm_stream_t stream);
 

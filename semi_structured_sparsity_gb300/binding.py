@@ -26,10 +26,13 @@ EXPORTS = ("maskllm_prior_init", "maskllm_forward", "maskllm_backward",
            "maskllm_hard_compress", "maskllm_decompress", "maskllm_noise_words",
            "maskllm_prior_init_batched", "maskllm_forward_batched", "maskllm_backward_batched",
            "maskllm_hard_compress_batched", "maskllm_prior_from_mask", "maskllm_mask_stats",
-           "maskllm_set_wait_timeout",
+           "maskllm_perm_shift", "maskllm_perm_metric", "maskllm_permute_columns",
+           "maskllm_perm_swap_gains", "maskllm_perm_search", "maskllm_set_wait_timeout",
            "maskllm_test_withhold_loads", "maskllm_device_status", "maskllm_status_string",
-           "maskllm_last_cuda_error")
+           "maskllm_last_cuda_error", "maskllm_perm_workspace_bytes")
 MAX_BATCH = 16
+PERM_BAD_PERMUTATION = -1   # maskllm_perm_search / maskllm_perm_swap_gains outcome codes
+PERM_NONFINITE = -2
 
 
 class maskllm_rng(C.Structure):
@@ -80,8 +83,15 @@ def lib() -> C.CDLL:
         L.maskllm_mask_stats.argtypes = [vp, vp, i64, i64, f32, f32, maskllm_rng, vp, vp, vp, vp]
         L.maskllm_set_wait_timeout.argtypes = [u64]
         L.maskllm_test_withhold_loads.argtypes = [i32]
-        for fn in EXPORTS[:-2]:
+        L.maskllm_perm_shift.argtypes = [vp, i64, i64, vp, vp]
+        L.maskllm_perm_metric.argtypes = [vp, i64, i64, vp, vp, vp, vp]
+        L.maskllm_permute_columns.argtypes = [vp, i64, i64, vp, vp, vp]
+        L.maskllm_perm_swap_gains.argtypes = [vp, i64, i64, vp, vp, i64, vp, vp, vp, vp]
+        L.maskllm_perm_search.argtypes = [vp, i64, i64, vp, i32, vp, i64, vp, vp, vp, vp, vp]
+        for fn in EXPORTS[:-3]:
             getattr(L, fn).restype = st
+        L.maskllm_perm_workspace_bytes.argtypes = [i64, i64]
+        L.maskllm_perm_workspace_bytes.restype = i64
         L.maskllm_status_string.argtypes = [st]
         L.maskllm_status_string.restype = C.c_char_p
         L.maskllm_last_cuda_error.argtypes = []
@@ -307,3 +317,88 @@ def maskllm_mask_stats(logits, tau, kappa, rng, prev_idx=None, idx_out=None, wan
         _ptr(logits), _ptr(prev_idx), rows, cols, tau, kappa, _rng(rng), _ptr(idx_out), _ptr(l1),
         _ptr(mp), _stream(stream)))
     return idx_out, l1, mp
+
+
+# ---------------------------------------------------------------------------
+# channel permutation before pruning
+# ---------------------------------------------------------------------------
+
+def _perm(perm, cols):
+    return _need(perm, "perm", torch.int32, (cols,))
+
+
+def maskllm_perm_shift(W, stream=None):
+    """int32 [1] device tensor: the fixed-point shift of W (INT32_MIN if W is
+    not finite)."""
+    rows, cols = W.shape
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    out = torch.empty((4,), dtype=torch.int32, device=W.device)   # 16-byte slot
+    _check("maskllm_perm_shift", lib().maskllm_perm_shift(_ptr(W), rows, cols, _ptr(out),
+                                                          _stream(stream)))
+    return out[:1]
+
+
+def maskllm_perm_metric(W, perm, shift, stream=None):
+    """int64 [1] device tensor: the fixed-point kept magnitude of perm."""
+    rows, cols = W.shape
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    _perm(perm, cols)
+    out = torch.empty((2,), dtype=torch.int64, device=W.device)
+    _check("maskllm_perm_metric", lib().maskllm_perm_metric(
+        _ptr(W), rows, cols, _ptr(perm), _ptr(shift), _ptr(out), _stream(stream)))
+    return out[:1]
+
+
+def maskllm_permute_columns(W, perm, W_out=None, stream=None):
+    rows, cols = W.shape
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    _perm(perm, cols)
+    W_out = _out(W_out, "W_out", torch.bfloat16, (rows, cols), W)
+    _check("maskllm_permute_columns", lib().maskllm_permute_columns(
+        _ptr(W), rows, cols, _ptr(perm), _ptr(W_out), _stream(stream)))
+    return W_out
+
+
+def maskllm_perm_workspace_bytes(rows: int, cols: int) -> int:
+    return int(lib().maskllm_perm_workspace_bytes(rows, cols))
+
+
+def _workspace(workspace, rows, cols, like):
+    need = maskllm_perm_workspace_bytes(rows, cols)
+    if need <= 0:
+        raise MaskLLMError("maskllm_perm_workspace_bytes", 2)
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=like.device)
+    return workspace
+
+
+def maskllm_perm_swap_gains(W, perm, workspace=None, stream=None):
+    """Returns (gains int64 [cols, cols], info int32 [1], shift int32 [1])."""
+    rows, cols = W.shape
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    _perm(perm, cols)
+    workspace = _workspace(workspace, rows, cols, W)
+    gains = torch.empty((cols, cols), dtype=torch.int64, device=W.device)
+    small = torch.zeros((8,), dtype=torch.int32, device=W.device)   # info, shift in 16-byte slots
+    _check("maskllm_perm_swap_gains", lib().maskllm_perm_swap_gains(
+        _ptr(W), rows, cols, _ptr(perm), _ptr(workspace), workspace.numel(), _ptr(gains),
+        _ptr(small), small.data_ptr() + 16, _stream(stream)))
+    return gains, small[0:1], small[4:5]
+
+
+def maskllm_perm_search(W, perm, max_swaps, workspace=None, log=True, stream=None):
+    """Steepest-ascent channel-swap search; perm (int32 [cols], device) is
+    updated in place.  Returns (n_swaps int32 [1], swaps int32 [max_swaps, 2]
+    | None, gains int64 [max_swaps] | None, shift int32 [1])."""
+    rows, cols = W.shape
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    _perm(perm, cols)
+    workspace = _workspace(workspace, rows, cols, W)
+    m = max(int(max_swaps), 1)
+    swaps = torch.zeros((m, 2), dtype=torch.int32, device=W.device) if log else None
+    gains = torch.zeros((m,), dtype=torch.int64, device=W.device) if log else None
+    small = torch.zeros((8,), dtype=torch.int32, device=W.device)   # n_swaps, shift
+    _check("maskllm_perm_search", lib().maskllm_perm_search(
+        _ptr(W), rows, cols, _ptr(perm), int(max_swaps), _ptr(workspace), workspace.numel(),
+        _ptr(swaps), _ptr(gains), _ptr(small), small.data_ptr() + 16, _stream(stream)))
+    return small[0:1], swaps, gains, small[4:5]

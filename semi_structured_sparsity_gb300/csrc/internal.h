@@ -70,6 +70,43 @@ cudaError_t stream_mask_stats(const Device& d, const StreamMatrix* m, int n, flo
 cudaError_t launch_prior_from_mask(const Device& d, const uint32_t* meta, int64_t rows,
                                    int64_t cols, float high, float low, float* logits,
                                    cudaStream_t s);
+// ---- channel permutation before pruning (kernels_perm.cu) -----------------
+
+constexpr int32_t kPermBadPermutation = -1;   // search / gains outcome codes
+constexpr int32_t kPermNonFinite = -2;
+constexpr int32_t kPermShiftNonFinite = -2147483647 - 1;   // shift of a non-finite matrix
+constexpr int64_t kPermMaxCols = 32768;
+constexpr int64_t kPermMaxRows = int64_t(1) << 24;
+
+// Control block of one search or gains call, in the caller's workspace.
+struct PermCtl {
+  unsigned long long key;   // best swap of the step (0: none)
+  uint32_t maxbits;         // largest |w| bit pattern
+  uint32_t flags;           // bit 0: bad permutation
+  int32_t shift;
+  int32_t code;             // 0, kPermBadPermutation or kPermNonFinite
+  int32_t done;
+  int32_t n_swaps;
+  int32_t rec_a, rec_b;     // the swap applied in this step
+};
+
+int64_t perm_workspace_bytes(int64_t rows, int64_t cols);
+cudaError_t perm_search(const Device& d, const uint16_t* W, int64_t rows, int64_t cols,
+                        int32_t* perm, int32_t max_swaps, void* workspace, int32_t* swaps_out,
+                        int64_t* gains_out, int32_t* n_swaps_out, int32_t* shift_out,
+                        cudaStream_t s);
+cudaError_t perm_swap_gains(const Device& d, const uint16_t* W, int64_t rows, int64_t cols,
+                            const int32_t* perm, void* workspace, int64_t* gains_out,
+                            int32_t* info_out, int32_t* shift_out, cudaStream_t s);
+cudaError_t perm_shift(const Device& d, const uint16_t* W, int64_t rows, int64_t cols,
+                       int32_t* shift_out, cudaStream_t s);
+cudaError_t perm_metric(const Device& d, const uint16_t* W, int64_t rows, int64_t cols,
+                        const int32_t* perm, const int32_t* shift, uint64_t* metric_out,
+                        cudaStream_t s);
+cudaError_t permute_columns(const Device& d, const uint16_t* W, int64_t rows, int64_t cols,
+                            const int32_t* perm, uint16_t* W_out, cudaStream_t s);
+cudaError_t read_and_clear_perm_error(cudaStream_t s, uint32_t* value);
+
 void stream_set_wait_ns(uint64_t ns);
 uint64_t stream_wait_ns();
 void stream_set_withhold_loads(int on);

@@ -503,6 +503,135 @@ maskllm_status maskllm_mask_stats(const float* logits, const uint8_t* prev_idx, 
                                                     {rng.seed, rng.step, rng.tensor_id}, stream));
 }
 
+}  // extern "C"
+
+namespace maskllm {
+namespace {
+
+maskllm_status check_perm_shape(int64_t rows, int64_t cols) {
+  MK_TRY(check_shape(rows, cols));
+  if (cols > kPermMaxCols || rows > kPermMaxRows) return MASKLLM_ERR_SHAPE;
+  return MASKLLM_OK;
+}
+
+}  // namespace
+}  // namespace maskllm
+
+extern "C" {
+
+maskllm_status maskllm_perm_shift(const uint16_t* W, int64_t rows, int64_t cols,
+                                  int32_t* shift_out, maskllm_stream_t stream) {
+  const void* ptrs[] = {W, shift_out};
+  MK_TRY(maskllm::check_ptrs(ptrs, 2));
+  MK_TRY(maskllm::check_perm_shape(rows, cols));
+  maskllm::Spans sp;
+  sp.input(W, 2 * static_cast<uint64_t>(rows) * cols);
+  sp.output(shift_out, 4);
+  MK_TRY(sp.check());
+  maskllm::Device d;
+  cudaError_t e = maskllm::current_device(&d);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
+  return maskllm::finish(maskllm::perm_shift(d, W, rows, cols, shift_out, stream));
+}
+
+maskllm_status maskllm_perm_metric(const uint16_t* W, int64_t rows, int64_t cols,
+                                   const int32_t* perm, const int32_t* shift,
+                                   uint64_t* metric_out, maskllm_stream_t stream) {
+  const void* ptrs[] = {W, perm, shift, metric_out};
+  MK_TRY(maskllm::check_ptrs(ptrs, 4));
+  MK_TRY(maskllm::check_perm_shape(rows, cols));
+  maskllm::Spans sp;
+  sp.input(W, 2 * static_cast<uint64_t>(rows) * cols);
+  sp.input(perm, 4 * static_cast<uint64_t>(cols));
+  sp.input(shift, 4);
+  sp.output(metric_out, 8);
+  MK_TRY(sp.check());
+  maskllm::Device d;
+  cudaError_t e = maskllm::current_device(&d);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
+  return maskllm::finish(maskllm::perm_metric(d, W, rows, cols, perm, shift, metric_out, stream));
+}
+
+maskllm_status maskllm_permute_columns(const uint16_t* W, int64_t rows, int64_t cols,
+                                       const int32_t* perm, uint16_t* W_out,
+                                       maskllm_stream_t stream) {
+  const void* ptrs[] = {W, perm, W_out};
+  MK_TRY(maskllm::check_ptrs(ptrs, 3));
+  MK_TRY(maskllm::check_perm_shape(rows, cols));
+  const uint64_t n = static_cast<uint64_t>(rows) * cols;
+  maskllm::Spans sp;
+  sp.input(W, 2 * n);
+  sp.input(perm, 4 * static_cast<uint64_t>(cols));
+  sp.output(W_out, 2 * n);
+  MK_TRY(sp.check());
+  maskllm::Device d;
+  cudaError_t e = maskllm::current_device(&d);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
+  return maskllm::finish(maskllm::permute_columns(d, W, rows, cols, perm, W_out, stream));
+}
+
+int64_t maskllm_perm_workspace_bytes(int64_t rows, int64_t cols) {
+  if (maskllm::check_perm_shape(rows, cols) != MASKLLM_OK) return 0;
+  return maskllm::perm_workspace_bytes(rows, cols);
+}
+
+maskllm_status maskllm_perm_swap_gains(const uint16_t* W, int64_t rows, int64_t cols,
+                                       const int32_t* perm, void* workspace,
+                                       int64_t workspace_bytes, int64_t* gains_out,
+                                       int32_t* info_out, int32_t* shift_out,
+                                       maskllm_stream_t stream) {
+  const void* ptrs[] = {W, perm, workspace, gains_out, info_out};
+  MK_TRY(maskllm::check_ptrs(ptrs, 5));
+  MK_TRY(maskllm::check_optional(shift_out));
+  MK_TRY(maskllm::check_perm_shape(rows, cols));
+  const int64_t need = maskllm::perm_workspace_bytes(rows, cols);
+  if (workspace_bytes < need) return MASKLLM_ERR_INVALID_ARG;
+  maskllm::Spans sp;
+  sp.input(W, 2 * static_cast<uint64_t>(rows) * cols);
+  sp.input(perm, 4 * static_cast<uint64_t>(cols));
+  sp.output(workspace, static_cast<uint64_t>(need));
+  sp.output(gains_out, 8 * static_cast<uint64_t>(cols) * cols);
+  sp.output(info_out, 4);
+  sp.output(shift_out, 4);
+  MK_TRY(sp.check());
+  maskllm::Device d;
+  cudaError_t e = maskllm::current_device(&d);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
+  return maskllm::finish(maskllm::perm_swap_gains(d, W, rows, cols, perm, workspace, gains_out,
+                                                  info_out, shift_out, stream));
+}
+
+maskllm_status maskllm_perm_search(const uint16_t* W, int64_t rows, int64_t cols, int32_t* perm,
+                                   int32_t max_swaps, void* workspace, int64_t workspace_bytes,
+                                   int32_t* swaps_out, int64_t* gains_out,
+                                   int32_t* n_swaps_out, int32_t* shift_out,
+                                   maskllm_stream_t stream) {
+  const void* ptrs[] = {W, perm, workspace, n_swaps_out};
+  MK_TRY(maskllm::check_ptrs(ptrs, 4));
+  MK_TRY(maskllm::check_optional(swaps_out));
+  MK_TRY(maskllm::check_optional(gains_out));
+  MK_TRY(maskllm::check_optional(shift_out));
+  MK_TRY(maskllm::check_perm_shape(rows, cols));
+  if (max_swaps < 0) return MASKLLM_ERR_INVALID_ARG;
+  const int64_t need = maskllm::perm_workspace_bytes(rows, cols);
+  if (workspace_bytes < need) return MASKLLM_ERR_INVALID_ARG;
+  maskllm::Spans sp;
+  sp.input(W, 2 * static_cast<uint64_t>(rows) * cols);
+  sp.output(perm, 4 * static_cast<uint64_t>(cols));
+  sp.output(workspace, static_cast<uint64_t>(need));
+  sp.output(swaps_out, 8 * static_cast<uint64_t>(max_swaps));
+  sp.output(gains_out, 8 * static_cast<uint64_t>(max_swaps));
+  sp.output(n_swaps_out, 4);
+  sp.output(shift_out, 4);
+  MK_TRY(sp.check());
+  maskllm::Device d;
+  cudaError_t e = maskllm::current_device(&d);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
+  return maskllm::finish(maskllm::perm_search(d, W, rows, cols, perm, max_swaps, workspace,
+                                              swaps_out, gains_out, n_swaps_out, shift_out,
+                                              stream));
+}
+
 maskllm_status maskllm_set_wait_timeout(uint64_t nanoseconds) {
   maskllm::stream_set_wait_ns(nanoseconds);
   return MASKLLM_OK;
@@ -514,11 +643,13 @@ maskllm_status maskllm_test_withhold_loads(int32_t enable) {
 }
 
 maskllm_status maskllm_device_status(maskllm_stream_t stream) {
-  uint32_t a = 0, b = 0;
+  uint32_t a = 0, b = 0, c = 0;
   cudaError_t e = maskllm::read_and_clear_error_word(stream, &a);
   if (e == cudaSuccess) e = maskllm::read_and_clear_stream_error(stream, &b);
+  if (e == cudaSuccess) e = maskllm::read_and_clear_perm_error(stream, &c);
   if (e != cudaSuccess) return maskllm::cuda_fail(e);
-  return (a | b) != 0 ? MASKLLM_ERR_TIMEOUT : MASKLLM_OK;
+  if ((a | b) != 0) return MASKLLM_ERR_TIMEOUT;
+  return c != 0 ? MASKLLM_ERR_INVALID_ARG : MASKLLM_OK;
 }
 
 const char* maskllm_status_string(maskllm_status status) {

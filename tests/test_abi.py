@@ -158,3 +158,29 @@ def test_next_entry_points_validation(L):
     assert L.maskllm_mask_stats(A, None, 1, (1 << 24) + 32, 1.0, 1.0, r, None, None, Cc, None) == SHAPE
     assert L.maskllm_mask_stats(A, None, 4, 64, 0.0, 1.0, r, None, None, Cc, None) == INVALID
     assert L.maskllm_mask_stats(A, None, 4, 64, 1.0, 1.0, r, A + 64, None, None, None) == ALIAS
+
+
+def test_permutation_entry_points_validation(L):
+    ws = L.maskllm_perm_workspace_bytes(64, 128)
+    assert ws == 128 * 128 * 4 + 2 * 64 * 128 * 4 + 256 + 128 // 8
+    assert L.maskllm_perm_workspace_bytes(64, 48) == 0            # cols % 32
+    assert L.maskllm_perm_workspace_bytes(64, 32768 + 32) == 0    # cols above 32768
+    assert L.maskllm_perm_workspace_bytes((1 << 24) + 1, 32) == 0
+    big = 0x40000000
+    # shift / metric / permute: null, alignment, shape, alias
+    assert L.maskllm_perm_shift(A, 4, 64, None, None) == INVALID
+    assert L.maskllm_perm_shift(A, 4, 64, B + 4, None) == ALIGN
+    assert L.maskllm_perm_shift(A, 4, 64, A + 16, None) == ALIAS
+    assert L.maskllm_perm_metric(A, 4, 64, B, Cc, None, None) == INVALID
+    assert L.maskllm_perm_metric(A, 4, 64, B, Cc, B + 16, None) == ALIAS
+    assert L.maskllm_permute_columns(A, 4, 64, B, A, None) == ALIAS
+    assert L.maskllm_permute_columns(A, 4, 65536, B, Cc, None) == SHAPE
+    # gains: workspace too small, info missing, gains over the workspace
+    assert L.maskllm_perm_swap_gains(A, 64, 128, B, big, ws - 1, Cc, D, None, None) == INVALID
+    assert L.maskllm_perm_swap_gains(A, 64, 128, B, big, ws, Cc, None, None, None) == INVALID
+    assert L.maskllm_perm_swap_gains(A, 64, 128, B, big, ws, big + 64, D, None, None) == ALIAS
+    # search: negative max_swaps, perm inside W, logs over each other
+    assert L.maskllm_perm_search(A, 64, 128, B, -1, big, ws, None, None, D, None, None) == INVALID
+    assert L.maskllm_perm_search(A, 64, 128, A + 16, 5, big, ws, None, None, D, None, None) == ALIAS
+    assert L.maskllm_perm_search(A, 64, 128, B, 5, big, ws, Cc, Cc + 16, D, None, None) == ALIAS
+    assert L.maskllm_perm_search(A, 64, 128, B, 5, big, ws, Cc + 8, None, D, None, None) == ALIGN
