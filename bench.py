@@ -452,7 +452,64 @@ def run_extras(blk, peak, dev, reps=20):
         out[name] = {"us_per_block": round(sec * 1e6, 2), "GB_per_s": round(gbs, 1),
                      "frac_of_hbm": round(gbs / peak, 4), "bytes_per_weight": bpw,
                      "launches_per_block": len(blk.mats)}
+    out["perm_search"] = run_perm_search(blk, dev)
     return out
+
+
+def run_perm_search(blk, dev, steps=256, reps=3):
+    """Channel-permutation search on the block's first matrix (the q
+    projection): the call with 0 steps (set-up and the [cols, cols] swap-gain
+    table, an integer max-plus product over the rows: cols^2 * rows
+    max-and-add evaluations), and with `steps` steps, CUDA-event timed on the
+    launching stream (best of `reps`)."""
+    import torch
+    mk = blk.mk
+    L = mk.lib()
+    s = torch.cuda.current_stream(dev).cuda_stream
+    Wq = blk.mats[0]["x"].W
+    rows, cols = Wq.shape
+    ws = torch.empty((mk.maskllm_perm_workspace_bytes(rows, cols),), dtype=torch.uint8,
+                     device=dev)
+    ident = torch.arange(cols, dtype=torch.int32, device=dev)
+    perm = ident.clone()
+    swaps = torch.zeros((steps, 2), dtype=torch.int32, device=dev)
+    gains = torch.zeros((steps,), dtype=torch.int64, device=dev)
+    small = torch.zeros((8,), dtype=torch.int32, device=dev)
+
+    def timed(n):
+        best = None
+        for _ in range(reps):
+            perm.copy_(ident)
+            torch.cuda.synchronize(dev)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            st = L.maskllm_perm_search(Wq.data_ptr(), rows, cols, perm.data_ptr(), n,
+                                       ws.data_ptr(), ws.numel(), swaps.data_ptr(),
+                                       gains.data_ptr(), small.data_ptr(),
+                                       small.data_ptr() + 16, s)
+            b.record()
+            torch.cuda.synchronize(dev)
+            assert st == 0
+            t = a.elapsed_time(b) / 1e3
+            best = t if best is None else min(best, t)
+        return best
+
+    timed(0)
+    t0 = timed(0)
+    tn = timed(steps)
+    n = int(small[0].item())
+    shift = int(small[4].item())
+    shift_t = torch.tensor([shift, 0, 0, 0], dtype=torch.int32, device=dev)
+    m_start = int(mk.maskllm_perm_metric(Wq, ident, shift_t).item())
+    m_end = int(mk.maskllm_perm_metric(Wq, perm, shift_t).item())
+    evals = float(cols) * cols * rows
+    return {"matrix": [rows, cols], "table_build_us": round(t0 * 1e6, 1),
+            "table_evals_per_s": round(evals / t0, 1),
+            "steps": n, "us_per_step": round((tn - t0) / max(n, 1) * 1e6, 2),
+            "kept_magnitude_gain": round((m_end - m_start) / max(m_start, 1), 6),
+            "note": "evals = cols^2 * rows max-and-add; table_build includes the scan and "
+                    "set-up kernels"}
 
 
 def run_e2e(args, blk, ranks, dev):

@@ -185,17 +185,27 @@ __global__ void __launch_bounds__(256) perm_prepare_kernel(const uint16_t* __res
 // ---------------------------------------------------------------------------
 // E[a][b] = sum_r max(S[r][a], V[r][b]): 128 x 128 tiles of E per block, 16
 // rows of S and V per step through shared memory (double-buffered through
-// registers), 8 x 8 outputs per thread.  Two rows are folded per add
-// (acc += max(..) + max(..)), and the sums are exact (below 2^32 by k).
+// registers), 8 x 8 outputs per thread.  The sums are exact (below 2^32 by
+// the choice of k).
 // ---------------------------------------------------------------------------
 
 constexpr int kTile = 128;
 constexpr int kKStep = 16;
 
+// acc + x * one as an integer multiply-add.  The loop is bound by the
+// integer ALU pipe, which issues the max; with `one` a run-time 1 the adds go
+// to the FMA pipe instead of competing with the max for the ALU pipe.
+__device__ __forceinline__ uint32_t mad_u32(uint32_t x, uint32_t one, uint32_t acc) {
+  uint32_t r;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(one), "r"(acc));
+  return r;
+}
+
 __global__ void __launch_bounds__(256) perm_table_kernel(const uint32_t* __restrict__ S,
                                                          const uint32_t* __restrict__ V,
                                                          uint32_t* __restrict__ E, int64_t rows,
-                                                         int32_t cols, const PermCtl* ctl) {
+                                                         int32_t cols, uint32_t one,
+                                                         const PermCtl* ctl) {
   if (ctl->done) return;
   __shared__ __align__(16) uint32_t sS[2][kKStep][kTile];
   __shared__ __align__(16) uint32_t sV[2][kKStep][kTile];
@@ -262,7 +272,10 @@ __global__ void __launch_bounds__(256) perm_table_kernel(const uint32_t* __restr
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] += max(s0[i], v0[j]) + max(s1[i], v1[j]);
+        for (int j = 0; j < 8; ++j) {
+          acc[i][j] = mad_u32(max(s0[i], v0[j]), one, acc[i][j]);
+          acc[i][j] = mad_u32(max(s1[i], v1[j]), one, acc[i][j]);
+        }
     }
     if (kt + 1 < nk) stash(buf ^ 1);
     __syncthreads();
@@ -622,7 +635,7 @@ cudaError_t prepare_table(const Device& d, const uint16_t* W, int64_t rows, int6
       W, rows, static_cast<int32_t>(cols), perm, w.S, w.V, w.ctl);
   const int nt = static_cast<int>((cols + kTile - 1) / kTile);
   perm_table_kernel<<<dim3(nt, nt), 256, 0, s>>>(w.S, w.V, w.E, rows, static_cast<int32_t>(cols),
-                                                 w.ctl);
+                                                 1u, w.ctl);
   return cudaGetLastError();
 }
 
