@@ -277,6 +277,37 @@ maskllm_status maskllm_perm_search(const uint16_t* W, int64_t rows, int64_t cols
                                    int32_t* n_swaps_out, int32_t* shift_out,
                                    maskllm_stream_t stream);
 
+/* ---- Permutation search without caller memory ---------------------------
+ * Not part of the method: the papers have no counterpart.  Some callers
+ * cannot hand the library device memory: code that must not call
+ * cudaMalloc (or any allocator) at the point where it runs the search, for
+ * example a runtime that has reserved all device memory up front for its own
+ * pool, or a host program with no allocator of device memory of its own.
+ * For them, maskllm_perm_search_static runs maskllm_perm_search with its
+ * scratch in an array that the library itself holds in device memory:
+ * MASKLLM_PERM_SEARCH_STATIC_BYTES bytes, held by every GPU that loads the
+ * library until the process exits.  It allocates nothing and frees nothing.
+ *
+ * Arguments, results and outcome codes are those of maskllm_perm_search
+ * without workspace and workspace_bytes.  A shape whose
+ * maskllm_perm_workspace_bytes() exceeds MASKLLM_PERM_SEARCH_STATIC_BYTES
+ * (for example cols = 1024 with rows above 3583, or cols = 2048 with rows
+ * above 1023) returns MASKLLM_ERR_SHAPE and launches nothing.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, under a lock); make that first call before any stream capture
+ * begins.  Every call on a device shares the one array: each call zeroes what
+ * must start at zero and overwrites the rest, so nothing carries over from
+ * the previous call, but calls that overlap on the GPU (other streams, other
+ * host threads) race on the array and give wrong results.  Issue them in
+ * order, on one stream or with synchronisation between them. */
+#define MASKLLM_PERM_SEARCH_STATIC_BYTES (32LL * 1024 * 1024)
+
+maskllm_status maskllm_perm_search_static(const uint16_t* W, int64_t rows, int64_t cols,
+                                          int32_t* perm, int32_t max_swaps, int32_t* swaps_out,
+                                          int64_t* gains_out, int32_t* n_swaps_out,
+                                          int32_t* shift_out, maskllm_stream_t stream);
+
 /* ---- Batched calls ------------------------------------------------------
  * One launch processes up to MASKLLM_MAX_BATCH matrices (for example the
  * seven linears of a transformer block); longer lists are split into several

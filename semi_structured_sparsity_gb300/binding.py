@@ -27,12 +27,14 @@ EXPORTS = ("maskllm_prior_init", "maskllm_forward", "maskllm_backward",
            "maskllm_prior_init_batched", "maskllm_forward_batched", "maskllm_backward_batched",
            "maskllm_hard_compress_batched", "maskllm_prior_from_mask", "maskllm_mask_stats",
            "maskllm_perm_shift", "maskllm_perm_metric", "maskllm_permute_columns",
-           "maskllm_perm_swap_gains", "maskllm_perm_search", "maskllm_set_wait_timeout",
+           "maskllm_perm_swap_gains", "maskllm_perm_search", "maskllm_perm_search_static",
+           "maskllm_set_wait_timeout",
            "maskllm_test_withhold_loads", "maskllm_device_status", "maskllm_status_string",
            "maskllm_last_cuda_error", "maskllm_perm_workspace_bytes")
 MAX_BATCH = 16
 PERM_BAD_PERMUTATION = -1   # maskllm_perm_search / maskllm_perm_swap_gains outcome codes
 PERM_NONFINITE = -2
+PERM_SEARCH_STATIC_BYTES = 32 * 1024 * 1024   # the library-held scratch of the no-allocation search
 
 
 class maskllm_rng(C.Structure):
@@ -88,6 +90,7 @@ def lib() -> C.CDLL:
         L.maskllm_permute_columns.argtypes = [vp, i64, i64, vp, vp, vp]
         L.maskllm_perm_swap_gains.argtypes = [vp, i64, i64, vp, vp, i64, vp, vp, vp, vp]
         L.maskllm_perm_search.argtypes = [vp, i64, i64, vp, i32, vp, i64, vp, vp, vp, vp, vp]
+        L.maskllm_perm_search_static.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp]
         for fn in EXPORTS[:-3]:
             getattr(L, fn).restype = st
         L.maskllm_perm_workspace_bytes.argtypes = [i64, i64]
@@ -401,4 +404,23 @@ def maskllm_perm_search(W, perm, max_swaps, workspace=None, log=True, stream=Non
     _check("maskllm_perm_search", lib().maskllm_perm_search(
         _ptr(W), rows, cols, _ptr(perm), int(max_swaps), _ptr(workspace), workspace.numel(),
         _ptr(swaps), _ptr(gains), _ptr(small), small.data_ptr() + 16, _stream(stream)))
+    return small[0:1], swaps, gains, small[4:5]
+
+
+def maskllm_perm_search_static(W, perm, max_swaps, log=True, stream=None):
+    """maskllm_perm_search with its scratch in the library's own device array
+    (no allocation by the caller or the library); same results.  Returns
+    (n_swaps int32 [1], swaps | None, gains | None, shift int32 [1]).  The
+    result tensors here are allocated by torch for convenience; a caller that
+    cannot allocate passes its own buffers to the C function."""
+    rows, cols = W.shape
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    _perm(perm, cols)
+    m = max(int(max_swaps), 1)
+    swaps = torch.zeros((m, 2), dtype=torch.int32, device=W.device) if log else None
+    gains = torch.zeros((m,), dtype=torch.int64, device=W.device) if log else None
+    small = torch.zeros((8,), dtype=torch.int32, device=W.device)
+    _check("maskllm_perm_search_static", lib().maskllm_perm_search_static(
+        _ptr(W), rows, cols, _ptr(perm), int(max_swaps), _ptr(swaps), _ptr(gains), _ptr(small),
+        small.data_ptr() + 16, _stream(stream)))
     return small[0:1], swaps, gains, small[4:5]

@@ -13,6 +13,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "internal.h"
 #include "maskllm.h"
@@ -668,3 +669,71 @@ const char* maskllm_status_string(maskllm_status status) {
 const char* maskllm_last_cuda_error(void) { return maskllm::t_last_cuda_error; }
 
 }  // extern "C"
+
+// ---- Permutation search without caller memory -----------------------------
+// For callers that cannot allocate device memory themselves (see
+// maskllm_perm_search_static in maskllm.h): the search's scratch lives in a
+// fixed array of this library's own device memory.
+
+namespace maskllm {
+
+static __device__ __align__(256) unsigned char
+    g_perm_static_scratch[MASKLLM_PERM_SEARCH_STATIC_BYTES];
+
+namespace {
+
+std::mutex g_perm_static_mutex;
+void* g_perm_static_addr[kMaxDevices];   // the array's device address, per device
+
+// Device address of the array on device `dev` (the current device): looked
+// up once per device.  In host code the array's name is only a host-side
+// stand-in, never an address a kernel may use.
+cudaError_t perm_static_scratch(int dev, void** addr) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_perm_static_mutex);
+  if (g_perm_static_addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_perm_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_perm_static_addr[dev] = p;
+  }
+  *addr = g_perm_static_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace maskllm
+
+extern "C" maskllm_status maskllm_perm_search_static(const uint16_t* W, int64_t rows,
+                                                     int64_t cols, int32_t* perm,
+                                                     int32_t max_swaps, int32_t* swaps_out,
+                                                     int64_t* gains_out, int32_t* n_swaps_out,
+                                                     int32_t* shift_out,
+                                                     maskllm_stream_t stream) {
+  const void* ptrs[] = {W, perm, n_swaps_out};
+  MK_TRY(maskllm::check_ptrs(ptrs, 3));
+  MK_TRY(maskllm::check_optional(swaps_out));
+  MK_TRY(maskllm::check_optional(gains_out));
+  MK_TRY(maskllm::check_optional(shift_out));
+  MK_TRY(maskllm::check_perm_shape(rows, cols));
+  if (max_swaps < 0) return MASKLLM_ERR_INVALID_ARG;
+  if (maskllm::perm_workspace_bytes(rows, cols) > MASKLLM_PERM_SEARCH_STATIC_BYTES)
+    return MASKLLM_ERR_SHAPE;
+  maskllm::Spans sp;
+  sp.input(W, 2 * static_cast<uint64_t>(rows) * cols);
+  sp.output(perm, 4 * static_cast<uint64_t>(cols));
+  sp.output(swaps_out, 8 * static_cast<uint64_t>(max_swaps));
+  sp.output(gains_out, 8 * static_cast<uint64_t>(max_swaps));
+  sp.output(n_swaps_out, 4);
+  sp.output(shift_out, 4);
+  MK_TRY(sp.check());
+  maskllm::Device d;
+  cudaError_t e = maskllm::current_device(&d);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
+  void* scratch = nullptr;
+  e = maskllm::perm_static_scratch(d.ordinal, &scratch);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
+  return maskllm::finish(maskllm::perm_search(d, W, rows, cols, perm, max_swaps, scratch,
+                                              swaps_out, gains_out, n_swaps_out, shift_out,
+                                              stream));
+}

@@ -184,3 +184,13 @@ def test_permutation_entry_points_validation(L):
     assert L.maskllm_perm_search(A, 64, 128, A + 16, 5, big, ws, None, None, D, None, None) == ALIAS
     assert L.maskllm_perm_search(A, 64, 128, B, 5, big, ws, Cc, Cc + 16, D, None, None) == ALIAS
     assert L.maskllm_perm_search(A, 64, 128, B, 5, big, ws, Cc + 8, None, D, None, None) == ALIGN
+
+
+def test_no_alloc_search_validation(L):
+    # the library-held scratch holds cols = 1024 up to 3583 rows
+    assert L.maskllm_perm_search_static(A, 3584, 1024, B, 5, None, None, D, None, None) == SHAPE
+    assert L.maskllm_perm_search_static(A, 64, 4096, B, 5, None, None, D, None, None) == SHAPE
+    assert L.maskllm_perm_search_static(A, 64, 128, B, -1, None, None, D, None, None) == INVALID
+    assert L.maskllm_perm_search_static(A, 64, 128, None, 5, None, None, D, None, None) == INVALID
+    assert L.maskllm_perm_search_static(A, 64, 128, A + 16, 5, None, None, D, None, None) == ALIAS
+    assert L.maskllm_perm_search_static(A, 64, 128, B, 5, Cc + 8, None, D, None, None) == ALIGN
