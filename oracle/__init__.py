@@ -322,3 +322,23 @@ def perm_search(W, perm, shift: int, max_swaps: int):
     n = int(lib().orc_perm_search(W, W.shape[0], W.shape[1], p, shift, max_swaps, _ptr(swaps),
                                   _ptr(gains)))
     return p, swaps[:n].copy(), gains[:n].copy()
+
+
+# ---------------------------------------------------------------------------
+# 2:4 sparse x dense product
+# ---------------------------------------------------------------------------
+
+def spmm(values, meta, M: int, K: int, B):
+    """C = A B^T in float64, A the [M, K] matrix stored as 2:4 values [M, K/2]
+    (bf16 bits) + metadata [M, K/32] (the orc_hard_compress layout), B dense
+    bf16 bits [N, K] ("Accelerating Sparse Deep Neural Networks", Sec. 3.2:
+    the sparse tensor core multiplies a 2:4 sparse first operand by a dense
+    second operand into a dense result).  Returns (C, S) with S = sum over k
+    of |A[m,k] B[n,k]|, the scale of the rounding error of any summation
+    order.  The product itself is numpy's float64 matmul of the decompressed
+    matrix: every bf16 product is exact in binary64 and the sums are rounded
+    only at binary64 precision, far below the fp32 accumulation error of any
+    single-precision kernel."""
+    A = bf16_to_f64(decompress(values, meta, M, K))
+    Bf = bf16_to_f64(np.asarray(B, np.uint16).reshape(-1, K))
+    return A @ Bf.T, np.abs(A) @ np.abs(Bf).T

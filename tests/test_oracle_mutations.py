@@ -62,6 +62,8 @@ MUTATIONS = {
     "perm_fixed_round": ("return (uint32_t)floor(ldexp(", "return (uint32_t)nearbyint(ldexp("),
     "perm_tie_rule": ("        if (g > best) {", "        if (g >= best && g > 0) {"),
     "perm_gain_sign": ("  return after - before;", "  return before - after;"),
+    "decompress_positions": ("const int i = (int)(code & 3u), j = (int)(code >> 2);",
+                             "const int j = (int)(code & 3u), i = (int)(code >> 2);"),
     "perm_swap_restore": ("  perm[b] = perm[a];\n  perm[a] = t;\n  return after",
                           "  perm[a] = t;\n  return after"),
 }
@@ -83,7 +85,8 @@ def _run_mutant(tmp_root, name, old, new):
     for fn in ("__init__.py", "workloads.py"):
         shutil.copy(os.path.join(ROOT, pkg, fn), os.path.join(d, pkg, fn))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        "tests/test_oracle_pins.py", "tests/test_oracle_perm_pins.py"], cwd=d, capture_output=True, text=True,
+                        "tests/test_oracle_pins.py", "tests/test_oracle_perm_pins.py",
+                        "tests/test_oracle_spmm_pins.py"], cwd=d, capture_output=True, text=True,
                        timeout=600)
     return name, r.returncode, (r.stdout.strip().splitlines() or [""])[-1]
 
