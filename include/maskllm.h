@@ -277,6 +277,31 @@ maskllm_status maskllm_perm_search(const uint16_t* W, int64_t rows, int64_t cols
                                    int32_t* n_swaps_out, int32_t* shift_out,
                                    maskllm_stream_t stream);
 
+/* ---- 2:4 sparse x dense product ------------------------------------------
+ * "Accelerating Sparse Deep Neural Networks", Sec. 3.2: the sparse tensor
+ * core multiplies a 2:4 sparse first operand by a dense second operand into
+ * a dense result, skipping the zeros (twice the math rate of the dense
+ * product); Sec. 3.1: the sparse operand is stored as its kept values plus
+ * 2-bit positions.
+ *
+ *   C[m, n] = sum over k of A[m, k] * B[n, k]      (C = A B^T)
+ *
+ *   values  in   bf16 [M, K/2] and
+ *   meta    in   u32 [M, K/32]: A in the layout maskllm_hard_compress writes
+ *                (group g of row m keeps values[m, 2g], values[m, 2g+1] at
+ *                positions i < j given by the 4-bit code i | j << 2 at bits
+ *                4(g % 8) of meta[m, g / 8]); codes must name two distinct
+ *                positions (the six candidates)
+ *   B       in   bf16 [N, K] row-major (for a linear layer: the N input rows)
+ *   C       out  fp32 [M, N] row-major
+ * Products are exact in fp32; they are summed in fp32 on the tensor cores in
+ * an order of their own.  M, N >= 1, K >= 32, K % 32 == 0, M, N < 2^31,
+ * K < 2^31.  A bounded wait that gives up makes the next
+ * maskllm_device_status() return MASKLLM_ERR_TIMEOUT; MASKLLM_ERR_CUDA if the
+ * driver cannot describe the operands to the copy engine. */
+maskllm_status maskllm_spmm(const uint16_t* values, const uint32_t* meta, int64_t M, int64_t K,
+                            const uint16_t* B, int64_t N, float* C, maskllm_stream_t stream);
+
 /* ---- Permutation search without caller memory ---------------------------
  * Not part of the method: the papers have no counterpart.  Some callers
  * cannot hand the library device memory: code that must not call

@@ -28,6 +28,7 @@ EXPORTS = ("maskllm_prior_init", "maskllm_forward", "maskllm_backward",
            "maskllm_hard_compress_batched", "maskllm_prior_from_mask", "maskllm_mask_stats",
            "maskllm_perm_shift", "maskllm_perm_metric", "maskllm_permute_columns",
            "maskllm_perm_swap_gains", "maskllm_perm_search", "maskllm_perm_search_static",
+           "maskllm_spmm",
            "maskllm_set_wait_timeout",
            "maskllm_test_withhold_loads", "maskllm_device_status", "maskllm_status_string",
            "maskllm_last_cuda_error", "maskllm_perm_workspace_bytes")
@@ -91,6 +92,7 @@ def lib() -> C.CDLL:
         L.maskllm_perm_swap_gains.argtypes = [vp, i64, i64, vp, vp, i64, vp, vp, vp, vp]
         L.maskllm_perm_search.argtypes = [vp, i64, i64, vp, i32, vp, i64, vp, vp, vp, vp, vp]
         L.maskllm_perm_search_static.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp]
+        L.maskllm_spmm.argtypes = [vp, vp, i64, i64, vp, i64, vp, vp]
         for fn in EXPORTS[:-3]:
             getattr(L, fn).restype = st
         L.maskllm_perm_workspace_bytes.argtypes = [i64, i64]
@@ -424,3 +426,22 @@ def maskllm_perm_search_static(W, perm, max_swaps, log=True, stream=None):
         _ptr(W), rows, cols, _ptr(perm), int(max_swaps), _ptr(swaps), _ptr(gains), _ptr(small),
         small.data_ptr() + 16, _stream(stream)))
     return small[0:1], swaps, gains, small[4:5]
+
+
+# ---------------------------------------------------------------------------
+# 2:4 sparse x dense product
+# ---------------------------------------------------------------------------
+
+def maskllm_spmm(values, meta, B, C=None, stream=None):
+    """C [M, N] fp32 = A B^T with A given as maskllm_hard_compress output
+    (values bf16 [M, K/2], meta int32 [M, K/32]) and B bf16 [N, K]."""
+    M, half = values.shape
+    K = 2 * half
+    N = B.shape[0]
+    _need(values, "values", torch.bfloat16, (M, half))
+    _need(meta, "meta", torch.int32, (M, K // 32))
+    _need(B, "B", torch.bfloat16, (N, K))
+    C = _out(C, "C", torch.float32, (M, N), values)
+    _check("maskllm_spmm", lib().maskllm_spmm(_ptr(values), _ptr(meta), M, K, _ptr(B), N, _ptr(C),
+                                              _stream(stream)))
+    return C

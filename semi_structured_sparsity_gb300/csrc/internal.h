@@ -107,6 +107,15 @@ cudaError_t permute_columns(const Device& d, const uint16_t* W, int64_t rows, in
                             const int32_t* perm, uint16_t* W_out, cudaStream_t s);
 cudaError_t read_and_clear_perm_error(cudaStream_t s, uint32_t* value);
 
+// ---- 2:4 sparse x dense product (kernels_spmm.cu) ------------------------
+// C [M, N] fp32 = A B^T, A as values bf16 [M, K/2] + codes u32 [M, K/32],
+// B bf16 [N, K].  Returns cudaErrorInvalidValue when the tensor maps cannot
+// be encoded.
+cudaError_t spmm(const Device& d, const uint16_t* values, const uint32_t* meta, int64_t M,
+                 int64_t K, const uint16_t* B, int64_t N, float* C, uint64_t wait_ns,
+                 cudaStream_t s);
+cudaError_t read_and_clear_spmm_error(cudaStream_t s, uint32_t* value);
+
 void stream_set_wait_ns(uint64_t ns);
 uint64_t stream_wait_ns();
 void stream_set_withhold_loads(int on);

@@ -647,9 +647,11 @@ maskllm_status maskllm_device_status(maskllm_stream_t stream) {
   uint32_t a = 0, b = 0, c = 0;
   cudaError_t e = maskllm::read_and_clear_error_word(stream, &a);
   if (e == cudaSuccess) e = maskllm::read_and_clear_stream_error(stream, &b);
+  uint32_t g = 0;
   if (e == cudaSuccess) e = maskllm::read_and_clear_perm_error(stream, &c);
+  if (e == cudaSuccess) e = maskllm::read_and_clear_spmm_error(stream, &g);
   if (e != cudaSuccess) return maskllm::cuda_fail(e);
-  if ((a | b) != 0) return MASKLLM_ERR_TIMEOUT;
+  if ((a | b | g) != 0) return MASKLLM_ERR_TIMEOUT;
   return c != 0 ? MASKLLM_ERR_INVALID_ARG : MASKLLM_OK;
 }
 
@@ -669,6 +671,27 @@ const char* maskllm_status_string(maskllm_status status) {
 const char* maskllm_last_cuda_error(void) { return maskllm::t_last_cuda_error; }
 
 }  // extern "C"
+
+extern "C" maskllm_status maskllm_spmm(const uint16_t* values, const uint32_t* meta, int64_t M,
+                                       int64_t K, const uint16_t* B, int64_t N, float* C,
+                                       maskllm_stream_t stream) {
+  const void* ptrs[] = {values, meta, B, C};
+  MK_TRY(maskllm::check_ptrs(ptrs, 4));
+  if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return MASKLLM_ERR_SHAPE;
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (M > lim || N > lim || K > lim || (M + 127) / 128 > 65535) return MASKLLM_ERR_SHAPE;
+  maskllm::Spans sp;
+  sp.input(values, static_cast<uint64_t>(M) * static_cast<uint64_t>(K));
+  sp.input(meta, static_cast<uint64_t>(M) * static_cast<uint64_t>(K) / 8);
+  sp.input(B, 2 * static_cast<uint64_t>(N) * static_cast<uint64_t>(K));
+  sp.output(C, 4 * static_cast<uint64_t>(M) * static_cast<uint64_t>(N));
+  MK_TRY(sp.check());
+  maskllm::Device d;
+  cudaError_t e = maskllm::current_device(&d);
+  if (e != cudaSuccess) return maskllm::cuda_fail(e);
+  return maskllm::finish(
+      maskllm::spmm(d, values, meta, M, K, B, N, C, maskllm::stream_wait_ns(), stream));
+}
 
 // ---- Permutation search without caller memory -----------------------------
 // For callers that cannot allocate device memory themselves (see

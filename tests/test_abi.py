@@ -194,3 +194,12 @@ def test_no_alloc_search_validation(L):
     assert L.maskllm_perm_search_static(A, 64, 128, None, 5, None, None, D, None, None) == INVALID
     assert L.maskllm_perm_search_static(A, 64, 128, A + 16, 5, None, None, D, None, None) == ALIAS
     assert L.maskllm_perm_search_static(A, 64, 128, B, 5, Cc + 8, None, D, None, None) == ALIGN
+
+
+def test_spmm_validation(L):
+    assert L.maskllm_spmm(A, B, 128, 64, Cc, 256, None, None) == INVALID
+    assert L.maskllm_spmm(A, B, 128, 48, Cc, 256, D, None) == SHAPE       # K % 32
+    assert L.maskllm_spmm(A, B, 0, 64, Cc, 256, D, None) == SHAPE
+    assert L.maskllm_spmm(A, B, 128, 64, Cc, 0, D, None) == SHAPE
+    assert L.maskllm_spmm(A + 8, B, 128, 64, Cc, 256, D, None) == ALIGN
+    assert L.maskllm_spmm(A, B, 128, 64, Cc, 256, Cc + 64, None) == ALIAS  # C over B
