@@ -453,6 +453,72 @@ def run_extras(blk, peak, dev, reps=20):
                      "frac_of_hbm": round(gbs / peak, 4), "bytes_per_weight": bpw,
                      "launches_per_block": len(blk.mats)}
     out["perm_search"] = run_perm_search(blk, dev)
+    out["spmm"] = run_spmm(blk, dev)
+    return out
+
+
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def run_spmm(blk, dev, n_tokens=4096, reps=20):
+    """2:4 sparse x dense product: the block's q projection as the hard mask
+    compressed it in the step, times n_tokens seeded bf16 activation rows
+    (C = A B^T, fp32 out), CUDA-event timed (median of reps).  Reported as
+    dense-equivalent TFLOP/s (2 M N K / t) against the sparse tensor peak,
+    twice the measured dense bf16 peak (the 2x math rate of the sparse tensor
+    cores); cuBLAS's dense product of the same (decompressed) matrix and, when
+    torch has it, cuSPARSELt's sparse product are timed beside it."""
+    import torch
+    from semi_structured_sparsity_gb300 import workloads as WL
+    mk = blk.mk
+    q = blk.mats[0]
+    vals, meta = q["values_out"], q["meta_out"]
+    M, half = vals.shape
+    K = 2 * half
+    Bt = WL.normal_bf16(n_tokens, K, 1.0, 4242, device=dev)
+    C = torch.empty((M, n_tokens), dtype=torch.float32, device=dev)
+
+    def med(fn):
+        # back-to-back launches (operands stay in L2, as in any GEMM
+        # benchmark): median over 5 runs of the mean of `reps` launches
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(5):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                fn()
+            b.record()
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b) / 1e3 / reps)
+        return statistics.median(ts)
+
+    flops = 2.0 * M * n_tokens * K
+    t = med(lambda: mk.maskllm_spmm(vals, meta, Bt, C=C))
+    peak, kind = bf16_peak()
+    out = {"M": M, "K": K, "N": n_tokens, "us": round(t * 1e6, 2),
+           "dense_equiv_tflops": round(flops / t / 1e12, 1),
+           "roofline": {"bound": "tensor", "peak": round(2 * peak, 1), "peak_kind":
+                        kind + " (2 x dense bf16)", "frac": round(flops / t / 1e12 / (2 * peak), 4)}}
+    Wd = mk.maskllm_decompress(vals, meta, M, K)
+    td = med(lambda: torch.matmul(Wd, Bt.t()))
+    out["cublas_dense_us"] = round(td * 1e6, 2)
+    try:
+        comp = torch._cslt_compress(Wd)
+        tc = med(lambda: torch._cslt_sparse_mm(comp, Bt.t()))
+        out["cusparselt_us"] = round(tc * 1e6, 2)
+    except Exception as e:   # torch built without cuSPARSELt
+        out["cusparselt_us"] = None
+        out["cusparselt_note"] = type(e).__name__
     return out
 
 
