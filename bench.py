@@ -46,7 +46,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gpu", "reference"), default="gpu")
     ap.add_argument("--workload", default="llama2_7b_block")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
@@ -360,7 +360,7 @@ def run_gpu(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, blk, ranks, dev)
+        e2e = run_e2e(args, blk, ranks, dev, only=only)
 
     cpu = None
     if not args.no_cpu_baseline and ranks.rank == 0 and ranks.world == 1:
@@ -578,11 +578,16 @@ def run_perm_search(blk, dev, steps=256, reps=3):
                     "set-up kernels"}
 
 
-def run_e2e(args, blk, ranks, dev):
+def run_e2e(args, blk, ranks, dev, only=None):
     """The same step through the C ABI with host buffers: every step copies
     W, logits and G from pinned host memory, runs the four kernels, and copies
-    every output back to pinned host memory."""
+    every output back to pinned host memory.  Steps are pipelined the way a
+    caller streaming many steps would: two sets of device buffers, the inputs
+    of step s + 1 copied in (one stream) while step s computes (a second) and
+    the outputs of step s - 1 are copied out (a third), ordered by events.
+    Every step's copies are inside the timed region."""
     import torch
+    sets = [blk, Block(blk.wl, layer=ranks.rank % max(blk.wl.layers, 1), device=dev, only=only)]
     host_in, host_out = [], []
     for m in blk.mats:
         x = m["x"]
@@ -591,33 +596,54 @@ def run_e2e(args, blk, ranks, dev):
                          for t in blk.outputs(m)])
     h2d = sum(t.numel() * t.element_size() for h in host_in for t in h)
     d2h = sum(t.numel() * t.element_size() for h in host_out for t in h)
-    stream = torch.cuda.current_stream(dev)
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
 
     def one(step):
-        for m, hin in zip(blk.mats, host_in):
-            x = m["x"]
-            for dst, src in zip((x.W, x.L, x.G), hin):
-                dst.copy_(src, non_blocking=True)
-        blk.run(step)
-        for m, hout in zip(blk.mats, host_out):
-            for dst, src in zip(hout, blk.outputs(m)):
-                dst.copy_(src, non_blocking=True)
+        x_i = step % 2
+        b = sets[x_i]
+        with torch.cuda.stream(s_in):
+            if step >= 2:
+                s_in.wait_event(ev["comp"][x_i])      # step - 2 has read these inputs
+            for m, hin in zip(b.mats, host_in):
+                x = m["x"]
+                for dst, src in zip((x.W, x.L, x.G), hin):
+                    dst.copy_(src, non_blocking=True)
+            ev["in"][x_i].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev["in"][x_i])
+            if step >= 2:
+                s_comp.wait_event(ev["out"][x_i])     # step - 2's outputs are out
+            b.run(step)
+            ev["comp"][x_i].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["comp"][x_i])
+            for m, hout in zip(b.mats, host_out):
+                for dst, src in zip(hout, b.outputs(m)):
+                    dst.copy_(src, non_blocking=True)
+            ev["out"][x_i].record(s_out)
 
-    one(0)
+    for w in range(2):
+        one(w)
     torch.cuda.synchronize(dev)
     ranks.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for s in range(args.e2e_steps):
-        one(s + 1)
-    t1.record(stream)
+    t0.record(s_in)
+    s_comp.wait_event(t0)
+    s_out.wait_event(t0)
+    for st in range(args.e2e_steps):
+        one(st + 2)
+    t1.record(s_out)
     torch.cuda.synchronize(dev)
     ranks.barrier()
     sec = ranks.max(t0.elapsed_time(t1) / 1e3)
+    del sets[1]
     return {"value": job_value(blk.weights, ranks.world, sec, args.e2e_steps),
             "unit": "weights/s", "steps": args.e2e_steps,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipelining": "2 device buffer sets; H2D, kernels and D2H of consecutive steps on "
+                          "3 streams"}
 
 
 # ---------------------------------------------------------------------------
