@@ -407,9 +407,10 @@ def run_gpu(args):
 
 def run_extras(blk, peak, dev, reps=20):
     """The entry points beyond the step, on the same resident block: logits
-    from a given mask (6.125 B/weight: codes in, logits out) and the
-    convergence diagnostics (6.5 B/weight: logits and previous draws in,
-    draws out), each over all matrices, CUDA-event timed."""
+    from a given mask (6.125 B/weight: codes in, logits out), the convergence
+    diagnostics (6.5 B/weight: logits and previous draws in, draws out) and
+    the forward with the diagnostics in the same pass (10.5 B/weight), each
+    over all matrices (one launch per matrix), CUDA-event timed."""
     import torch
     mk, wl = blk.mk, blk.wl
     L = mk.lib()
@@ -434,9 +435,22 @@ def run_extras(blk, peak, dev, reps=20):
                                       l1[i].data_ptr(), mp[i].data_ptr(), s)
             assert st == 0
 
+    w_out = [torch.empty_like(m["x"].W) for m in blk.mats]
+    row_sq = [torch.empty((m["x"].rows,), dtype=torch.float32, device=dev) for m in blk.mats]
+
+    def forward_stats(step):
+        for i, m in enumerate(blk.mats):
+            st = L.maskllm_forward_stats(m["W"].data_ptr(), m["logits"].data_ptr(),
+                                         draws[i].data_ptr(), m["x"].rows, m["x"].cols, wl.tau,
+                                         wl.kappa, mk.maskllm_rng(0, step, m["tensor_id"]),
+                                         w_out[i].data_ptr(), row_sq[i].data_ptr(),
+                                         nxt[i].data_ptr(), l1[i].data_ptr(), mp[i].data_ptr(), s)
+            assert st == 0
+
     out = {}
     for name, fn, bpw in (("prior_from_mask", lambda i: prior_from_mask(), 6.125),
-                          ("mask_stats", mask_stats, 6.5)):
+                          ("mask_stats", mask_stats, 6.5),
+                          ("forward_stats", forward_stats, 10.5)):
         for i in range(3):
             fn(i)
         torch.cuda.synchronize(dev)

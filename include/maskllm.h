@@ -333,6 +333,23 @@ maskllm_status maskllm_perm_search_static(const uint16_t* W, int64_t rows, int64
                                           int64_t* gains_out, int32_t* n_swaps_out,
                                           int32_t* shift_out, maskllm_stream_t stream);
 
+/* The forward and the convergence diagnostics of one step in a single pass
+ * (MaskLLM Fig. 5; the optional outputs of maskllm_forward): W_out and
+ * row_sq_out exactly as maskllm_forward computes them (bit-identical), and
+ * idx_out, l1_row_out, maxprob_row_out exactly as maskllm_mask_stats
+ * computes them for the same step.  The noisy logits z the forward forms
+ * give the draws, so the diagnostics cost a few instructions per group and
+ * 2 bytes of traffic per group instead of a second pass over the logits.
+ *   W, logits, W_out, row_sq_out   as maskllm_forward (row_sq_out nullable)
+ *   prev_idx, idx_out, l1_row_out, maxprob_row_out   as maskllm_mask_stats
+ *                                  (all nullable; l1_row_out needs prev_idx)
+ * cols <= 2^24. */
+maskllm_status maskllm_forward_stats(const uint16_t* W, const float* logits,
+                                     const uint8_t* prev_idx, int64_t rows, int64_t cols,
+                                     float tau, float kappa, maskllm_rng rng, uint16_t* W_out,
+                                     float* row_sq_out, uint8_t* idx_out, uint32_t* l1_row_out,
+                                     float* maxprob_row_out, maskllm_stream_t stream);
+
 /* ---- Batched calls ------------------------------------------------------
  * One launch processes up to MASKLLM_MAX_BATCH matrices (for example the
  * seven linears of a transformer block); longer lists are split into several

@@ -28,7 +28,7 @@ EXPORTS = ("maskllm_prior_init", "maskllm_forward", "maskllm_backward",
            "maskllm_hard_compress_batched", "maskllm_prior_from_mask", "maskllm_mask_stats",
            "maskllm_perm_shift", "maskllm_perm_metric", "maskllm_permute_columns",
            "maskllm_perm_swap_gains", "maskllm_perm_search", "maskllm_perm_search_static",
-           "maskllm_spmm",
+           "maskllm_spmm", "maskllm_forward_stats",
            "maskllm_set_wait_timeout",
            "maskllm_test_withhold_loads", "maskllm_device_status", "maskllm_status_string",
            "maskllm_last_cuda_error", "maskllm_perm_workspace_bytes")
@@ -93,6 +93,8 @@ def lib() -> C.CDLL:
         L.maskllm_perm_search.argtypes = [vp, i64, i64, vp, i32, vp, i64, vp, vp, vp, vp, vp]
         L.maskllm_perm_search_static.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp]
         L.maskllm_spmm.argtypes = [vp, vp, i64, i64, vp, i64, vp, vp]
+        L.maskllm_forward_stats.argtypes = [vp, vp, vp, i64, i64, f32, f32, maskllm_rng, vp, vp,
+                                            vp, vp, vp, vp]
         for fn in EXPORTS[:-3]:
             getattr(L, fn).restype = st
         L.maskllm_perm_workspace_bytes.argtypes = [i64, i64]
@@ -445,3 +447,28 @@ def maskllm_spmm(values, meta, B, C=None, stream=None):
     _check("maskllm_spmm", lib().maskllm_spmm(_ptr(values), _ptr(meta), M, K, _ptr(B), N, _ptr(C),
                                               _stream(stream)))
     return C
+
+
+def maskllm_forward_stats(W, logits, tau, kappa, rng, prev_idx=None, W_out=None, want_row_sq=True,
+                          want_idx=True, want_l1=None, want_maxprob=True, stream=None):
+    """The forward and the step's diagnostics in one pass.  Returns (W_out,
+    row_sq | None, idx | None, l1 int32 | None, maxprob | None); l1 holds
+    uint32 values in an int32 tensor."""
+    rows, cols = W.shape
+    g = cols // 4
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    _need(logits, "logits", torch.float32, (rows, g, 6))
+    if prev_idx is not None:
+        _need(prev_idx, "prev_idx", torch.uint8, (rows, g))
+    W_out = _out(W_out, "W_out", torch.bfloat16, (rows, cols), W)
+    dev = W.device
+    row_sq = torch.empty((rows,), dtype=torch.float32, device=dev) if want_row_sq else None
+    idx = torch.empty((rows, g), dtype=torch.uint8, device=dev) if want_idx else None
+    if want_l1 is None:
+        want_l1 = prev_idx is not None
+    l1 = torch.empty((rows,), dtype=torch.int32, device=dev) if want_l1 else None
+    mp = torch.empty((rows,), dtype=torch.float32, device=dev) if want_maxprob else None
+    _check("maskllm_forward_stats", lib().maskllm_forward_stats(
+        _ptr(W), _ptr(logits), _ptr(prev_idx), rows, cols, tau, kappa, _rng(rng), _ptr(W_out),
+        _ptr(row_sq), _ptr(idx), _ptr(l1), _ptr(mp), _stream(stream)))
+    return W_out, row_sq, idx, l1, mp

@@ -115,12 +115,18 @@ constexpr float kExpOffset = 64.0f;
 // four soft-mask numerators n_j = sum of e_c over the candidates keeping j:
 // position 0: c0 (0,1) c1 (0,2) c2 (0,3);  position 1: c0, c3 (1,2), c4 (1,3);
 // position 2: c1, c3, c5 (2,3);            position 3: c2, c4, c5.
-__device__ __forceinline__ void softmax6(const float L[kCand], const float g[kCand], float kappa,
-                                         float rho, float e[kCand], float& inv_sum,
-                                         float num[4]) {
-  float z[kCand];
+__device__ __forceinline__ void noisy_logits6(const float L[kCand], const float g[kCand],
+                                              float kappa, float rho, float y[kCand],
+                                              float z[kCand]) {
 #pragma unroll
-  for (int c = 0; c < kCand; ++c) z[c] = __fmul_rn(__fadd_rn(__fmul_rn(kappa, L[c]), g[c]), rho);
+  for (int c = 0; c < kCand; ++c) {
+    y[c] = __fmul_rn(kappa, L[c]);
+    z[c] = __fmul_rn(__fadd_rn(y[c], g[c]), rho);
+  }
+}
+
+__device__ __forceinline__ void softmax6_of_z(const float z[kCand], float e[kCand],
+                                              float& inv_sum, float num[4]) {
   const float m = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])), fmaxf(z[4], z[5]));
   const float shift = kExpOffset - __fmul_rn(m, kLog2e);
 #pragma unroll
@@ -133,6 +139,14 @@ __device__ __forceinline__ void softmax6(const float L[kCand], const float g[kCa
   num[2] = e[1] + e35;
   num[3] = e[2] + e45;
   inv_sum = rcp_approx(num[0] + e34 + e[5]);
+}
+
+__device__ __forceinline__ void softmax6(const float L[kCand], const float g[kCand], float kappa,
+                                         float rho, float e[kCand], float& inv_sum,
+                                         float num[4]) {
+  float y[kCand], z[kCand];
+  noisy_logits6(L, g, kappa, rho, y, z);
+  softmax6_of_z(z, e, inv_sum, num);
 }
 
 // Soft mask M_j = sum of p_c over the candidates keeping position j.

@@ -51,6 +51,8 @@ struct StreamMatrix {
   void* out0;         // prior: logits; forward: W'; backward: dlogits; compress: values
   void* out1;         // forward: row_sq (nullable); compress: codes
   void* out2;         // forward: probs (nullable); compress: idx (nullable)
+  void* out3 = nullptr;   // forward with diagnostics: L1 distance per row (u32)
+  void* out4 = nullptr;   // forward with diagnostics: max-probability sum per row (fp32)
   int64_t rows;
   int64_t cols;
   uint32_t tensor_id;
@@ -67,6 +69,11 @@ cudaError_t stream_hard_compress(const Device& d, const StreamMatrix* m, int n, 
 // out1 = L1 distance per row (u32, needs G); out2 = max-probability sum per row
 cudaError_t stream_mask_stats(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
                               RngArgs rng, cudaStream_t s);
+// The forward (out0 = W', out1 = row_sq) with the diagnostics of
+// stream_mask_stats in the same pass: G = previous draws, out2 = draws,
+// out3 = L1 per row, out4 = max-probability sum per row (all nullable).
+cudaError_t stream_forward_stats(const Device& d, const StreamMatrix* m, int n, float tau,
+                                 float kappa, RngArgs rng, cudaStream_t s);
 cudaError_t launch_prior_from_mask(const Device& d, const uint32_t* meta, int64_t rows,
                                    int64_t cols, float high, float low, float* logits,
                                    cudaStream_t s);

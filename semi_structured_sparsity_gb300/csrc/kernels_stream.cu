@@ -58,7 +58,9 @@ struct MatDesc {
   const void* G;          // bf16 [rows, cols] (backward)
   void* out0;             // prior: logits; forward: W'; backward: dlogits; compress: values
   void* out1;             // forward: row_sq; compress: codes
-  void* out2;             // forward: probs; compress: idx
+  void* out2;             // forward: probs; compress: idx; forward + stats: draws
+  void* out3;             // forward + stats: L1 per row
+  void* out4;             // forward + stats: max-probability sum per row
   int64_t rows;
   int64_t unit_begin;     // first unit of this matrix in the launch's unit list
   int64_t chunk_begin;    // first chunk of this matrix in the launch's chunk list
@@ -583,6 +585,91 @@ struct StatsOp : OpBase<GPT, 4> {
   }
 };
 
+// The forward with the convergence diagnostics in the same pass (the
+// optional outputs of the "MaskLLM" Fig. 5 quantities): the noisy logits z
+// the forward forms anyway give the draw (their first maximum), and the
+// scaled logits fl32(kappa * L) it forms on the way give the distribution's
+// largest probability.  W' and row_sq are computed exactly as in FwdOp; the
+// draws, L1 and max-probability exactly as in StatsOp.  Row quantities: 0
+// row_sq, 1 L1 distance, 2 max-probability sum (three floats in the
+// thread's consumed W slot).
+template <int GPT>
+struct FwdStatsOp : OpBase<GPT, 4> {
+  static constexpr bool kTable = true, kStaged = false, kWarpWide = false;
+  static constexpr bool kOutOverlapsInput = false;
+  static constexpr int kRowQuantities = 3;
+  static constexpr uint32_t kPartOffset = 0;
+  static constexpr uint32_t kPartStride = 8 * GPT;
+  static_assert(8 * GPT >= 12, "three row partials fit the thread's W slot");
+  __device__ static bool want_row(const MatDesc& d, int q) {
+    return q == 0 ? d.out1 != nullptr : (q == 1 ? (d.out3 != nullptr && d.G != nullptr)
+                                                 : d.out4 != nullptr);
+  }
+  __device__ static void write_row(const MatDesc& d, int64_t row, int q, float v) {
+    if (q == 0)
+      static_cast<float*>(d.out1)[row] = v;
+    else if (q == 1)
+      static_cast<uint32_t*>(d.out3)[row] = static_cast<uint32_t>(v);   // exact below 2^24
+    else
+      static_cast<float*>(d.out4)[row] = v;
+  }
+  static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
+  static constexpr uint32_t kOutOffset = 0;
+  static constexpr uint32_t kOutBytesPerGroup = 0;
+
+  __device__ static void issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
+    FwdOp<false, GPT>::issue(d, c, st, bar);
+  }
+
+  __device__ static void consume(const StreamParams& p, const MatDesc& d, const Chunk& c,
+                                 uint8_t* st, int t, const float* tab, float* acc) {
+    static_assert(GPT == 2, "draws are stored as one 16-bit pair per thread");
+    uint32_t w[2 * GPT], o[2 * GPT];
+    float L[6 * GPT];
+    load_w<GPT>(st, t, w);
+    load_l<GPT>(st + kChunkGroups * 8, t, L);
+    const int64_t unit = c.g0 / GPT + t;
+    const uint32_t prev = d.G != nullptr ? static_cast<const uint16_t*>(d.G)[unit] : 0u;
+    const uint64_t g0 = static_cast<uint64_t>(c.g0) + static_cast<uint64_t>(GPT * t);
+    uint32_t drawn = 0;
+#pragma unroll
+    for (int k = 0; k < GPT; ++k) {
+      const float* Lk = L + 6 * k;
+      float g[kCand], y[kCand], z[kCand], e[kCand], inv, num[4], M[4];
+      gumbel6(group_words(g0 + k, p.s.step, d.tensor_id, p.s.keys), tab, g);
+      noisy_logits6(Lk, g, p.s.kappa, p.s.rho, y, z);
+      softmax6_of_z(z, e, inv, num);
+      soft_mask4(num, inv, M);
+      const uint32_t w01 = w[2 * k], w23 = w[2 * k + 1];
+      const float x0 = __fmul_rn(bf16_lo(w01), M[0]);
+      const float x1 = __fmul_rn(bf16_hi(w01), M[1]);
+      const float x2 = __fmul_rn(bf16_lo(w23), M[2]);
+      const float x3 = __fmul_rn(bf16_hi(w23), M[3]);
+      o[2 * k] = pack_bf16x2_rn(x0, x1);
+      o[2 * k + 1] = pack_bf16x2_rn(x2, x3);
+      acc[0] = __fmaf_rn(x0, x0, acc[0]);
+      acc[0] = __fmaf_rn(x1, x1, acc[0]);
+      acc[0] = __fmaf_rn(x2, x2, acc[0]);
+      acc[0] = __fmaf_rn(x3, x3, acc[0]);
+      // diagnostics
+      const int s = first_argmax6(z);
+      drawn |= static_cast<uint32_t>(s) << (8 * k);
+      if (d.G != nullptr) {
+        const uint32_t q = (prev >> (8 * k)) & 7u;   // entries 6, 7 count as empty masks
+        acc[1] += static_cast<float>(
+            __popc(((kKeepBits >> (4 * s)) ^ (kKeepBits >> (4 * q))) & 0xFu));
+      }
+      const float my = fmaxf(fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3])), fmaxf(y[4], y[5]));
+      float sum = 0.f;
+#pragma unroll
+      for (int c6 = 0; c6 < kCand; ++c6) sum += ex2_approx((y[c6] - my) * kLog2e);
+      acc[2] += rcp_approx(sum);   // the largest term is 2^0 = 1
+    }
+    store_w_global<GPT>(d.out0, unit, o);
+    if (d.out2 != nullptr) static_cast<uint16_t*>(d.out2)[unit] = static_cast<uint16_t>(drawn);
+  }
+};
+
 // ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
@@ -723,7 +810,7 @@ __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
   it.init(&p, u0, u1);
   Chunk c;
   int64_t n = 0;
-  float acc[2] = {0.f, 0.f};   // per-row quantities of this thread
+  float acc[3] = {0.f, 0.f, 0.f};   // per-row quantities of this thread
   while (it.next(c)) {
     const int s = static_cast<int>(n % S);
     const bool got = mbar_wait_bounded(&full[s], static_cast<uint32_t>((n / S) & 1), p.wait_ns,
@@ -804,6 +891,8 @@ void describe(StreamParams& p, const StreamMatrix* mats, int n) {
     d.out0 = m.out0;
     d.out1 = m.out1;
     d.out2 = m.out2;
+    d.out3 = m.out3;
+    d.out4 = m.out4;
     d.rows = m.rows;
     d.gpr = static_cast<int32_t>(m.cols / 4);
     d.tensor_id = m.tensor_id;
@@ -858,6 +947,7 @@ static_assert(Layout<BwdOp<true, kGPT>>::kBytes <= 232448, "backward shared memo
 static_assert(Layout<PriorOp<kGPT>>::kBytes <= 232448, "prior shared memory");
 static_assert(Layout<CompressOp<kGPT>>::kBytes <= 232448, "compress shared memory");
 static_assert(Layout<StatsOp<kGPT>>::kBytes <= 232448, "stats shared memory");
+static_assert(Layout<FwdStatsOp<kGPT>>::kBytes <= 232448, "forward + stats shared memory");
 static_assert(sizeof(StreamParams) <= 4000, "kernel parameters");
 
 cudaError_t stream_prior_init(const Device& d, const StreamMatrix* m, int n, float scale,
@@ -898,6 +988,14 @@ cudaError_t stream_mask_stats(const Device& d, const StreamMatrix* m, int n, flo
   describe(p, m, n);
   p.s = scalars(tau, kappa, rng, 0.0f, 0.0f);
   return launch<StatsOp<kGPT>>(d, p, s);
+}
+
+cudaError_t stream_forward_stats(const Device& d, const StreamMatrix* m, int n, float tau,
+                                 float kappa, RngArgs rng, cudaStream_t s) {
+  StreamParams p;
+  describe(p, m, n);
+  p.s = scalars(tau, kappa, rng, 0.0f, 0.0f);
+  return launch<FwdStatsOp<kGPT>>(d, p, s);
 }
 
 void stream_set_wait_ns(uint64_t ns) { g_wait_ns = ns; }

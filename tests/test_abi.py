@@ -203,3 +203,14 @@ def test_spmm_validation(L):
     assert L.maskllm_spmm(A, B, 128, 64, Cc, 0, D, None) == SHAPE
     assert L.maskllm_spmm(A + 8, B, 128, 64, Cc, 256, D, None) == ALIGN
     assert L.maskllm_spmm(A, B, 128, 64, Cc, 256, Cc + 64, None) == ALIAS  # C over B
+
+
+def test_forward_stats_validation(L):
+    r = _rng()
+    f = L.maskllm_forward_stats
+    assert f(A, B, None, 4, 64, 1.0, 1.0, r, None, None, None, None, None, None) == INVALID
+    assert f(A, B, None, 4, 64, 1.0, 1.0, r, Cc, None, None, D, None, None) == INVALID   # L1 needs prev
+    assert f(A, B, None, 1, (1 << 24) + 32, 1.0, 1.0, r, Cc, None, None, None, None, None) == SHAPE
+    assert f(A, B, None, 4, 64, 0.0, 1.0, r, Cc, None, None, None, None, None) == INVALID
+    assert f(A, B, None, 4, 64, 1.0, 1.0, r, A + 16, None, None, None, None, None) == ALIAS
+    assert f(A, B, None, 4, 64, 1.0, 1.0, r, Cc, D + 4, None, None, None, None) == ALIGN

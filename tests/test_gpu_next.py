@@ -84,3 +84,44 @@ def test_mask_stats_validation():
     st = mk.lib().maskllm_mask_stats(L.data_ptr(), None, 4, 64, 1.0, 1.0, mk._rng((0, 0, 0)),
                                      None, l1.data_ptr(), None, None)
     assert st == 1   # the L1 distance needs the previous draws
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES)
+@pytest.mark.parametrize("tau,kappa", [(1.0, 3.0), (0.2, 500.0)])
+def test_forward_stats_is_forward_plus_stats(rows, cols, tau, kappa):
+    """The fused pass: W' and row_sq bit-identical to maskllm_forward (and
+    within the forward's tolerance of the oracle), draws / L1 / max
+    probability as maskllm_mask_stats and the oracle."""
+    from tests._helpers import ROWSQ_RTOL, assert_bf16_ulps, bits16
+    W, L, _ = wl.random_case(rows, cols, seed=3 * rows + cols, device="cuda")
+    rng_prev, rng = (9, 20, 4), (9, 21, 4)
+    prev, _, _ = mk.maskllm_mask_stats(L, tau, kappa, rng_prev)
+    Wo, rsq, idx, l1, mp = mk.maskllm_forward_stats(W, L, tau, kappa, rng, prev_idx=prev)
+    Wf = torch.empty_like(W)
+    rf = torch.empty((rows,), device="cuda")
+    mk.maskllm_forward(W, L, tau, kappa, rng, W_out=Wf, row_sq_out=rf)
+    sidx, sl1, smp = mk.maskllm_mask_stats(L, tau, kappa, rng, prev_idx=prev)
+    torch.cuda.synchronize()
+    assert torch.equal(Wo.view(torch.int16), Wf.view(torch.int16))
+    assert_close(rsq.cpu().numpy(), rf.cpu().numpy(), rtol=1e-6, atol=0, what="row_sq vs forward")
+    assert torch.equal(idx, sidx) and torch.equal(l1, sl1)
+    assert_close(mp.cpu().numpy(), smp.cpu().numpy(), rtol=1e-6, atol=0, what="max-prob vs stats")
+    Wb, Lh = bits16(W), L.cpu().numpy()
+    wW, wsq, _, _ = orc.forward(Wb, Lh, tau, kappa, *rng)
+    assert_bf16_ulps(bits16(Wo), wW)
+    assert_close(rsq.cpu().numpy(), wsq, rtol=ROWSQ_RTOL, atol=0, what="row_sq")
+    wprev, _, _ = orc.mask_stats(Lh, rows, cols, tau, kappa, *rng_prev)
+    widx, wl1, wmp = orc.mask_stats(Lh, rows, cols, tau, kappa, *rng, prev_idx=wprev)
+    assert_bits_equal(idx.cpu().numpy(), widx, "draws")
+    assert_bits_equal(l1.cpu().numpy().view(np.uint32), wl1.astype(np.uint32), "L1 per row")
+    assert_close(mp.cpu().numpy(), wmp, rtol=1e-5, atol=0, what="max-probability row sum")
+
+
+def test_forward_stats_optional_outputs():
+    W, L, _ = wl.random_case(40, 256, seed=5, device="cuda")
+    Wo, rsq, idx, l1, mp = mk.maskllm_forward_stats(W, L, 1.0, 3.0, (1, 2, 3), want_row_sq=False,
+                                                    want_idx=False, want_maxprob=False)
+    Wf = mk.maskllm_forward(W, L, 1.0, 3.0, (1, 2, 3))[0]
+    torch.cuda.synchronize()
+    assert rsq is None and idx is None and l1 is None and mp is None
+    assert torch.equal(Wo.view(torch.int16), Wf.view(torch.int16))
