@@ -247,8 +247,9 @@ maskllm_status maskllm_permute_columns(const uint16_t* W, int64_t rows, int64_t 
                                        maskllm_stream_t stream);
 
 /* Device scratch the two calls below need, in bytes (0 for a shape outside
- * the rules): a [cols, cols] and two [rows, cols] uint32 tables and a few
- * hundred bytes of control.  The caller owns it; it holds nothing between
+ * the rules): a [cols, cols] and two [rows, cols] uint32 tables, 8 bytes
+ * per 32 x 32 tile of the first's upper triangle, and a few hundred bytes of
+ * control.  The caller owns it; it holds nothing between
  * calls. */
 int64_t maskllm_perm_workspace_bytes(int64_t rows, int64_t cols);
 
@@ -317,7 +318,7 @@ maskllm_status maskllm_spmm(const uint16_t* values, const uint32_t* meta, int64_
  * without workspace and workspace_bytes.  A shape whose
  * maskllm_perm_workspace_bytes() exceeds MASKLLM_PERM_SEARCH_STATIC_BYTES
  * (for example cols = 1024 with rows above 3583, or cols = 2048 with rows
- * above 1023) returns MASKLLM_ERR_SHAPE and launches nothing.
+ * above 1022) returns MASKLLM_ERR_SHAPE and launches nothing.
  *
  * The first call on a device looks up the array's device address (once per
  * device, under a lock); make that first call before any stream capture

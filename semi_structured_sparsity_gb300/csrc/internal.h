@@ -88,6 +88,7 @@ constexpr int64_t kPermMaxRows = int64_t(1) << 24;
 // Control block of one search or gains call, in the caller's workspace.
 struct PermCtl {
   unsigned long long key;   // best swap of the step (0: none)
+  uint32_t tiles_done;      // tiles of the best-pair scan finished this step
   uint32_t maxbits;         // largest |w| bit pattern
   uint32_t flags;           // bit 0: bad permutation
   int32_t shift;

@@ -31,9 +31,9 @@
 // the rows, computed by a tiled kernel; after a swap of slots a and b the
 // columns a and b of V, hence of E, trade places, and S changes only for the
 // three group-mates of a and of b, whose six rows of E are recomputed.  One
-// search step is three kernels: best (the largest gain over all pairs, one
-// 64-bit atomic max per block), apply (the swap and the cheap updates), rows
-// (the six E rows).  All of them return at once when the search has stopped,
+// search step is three kernels: best (the largest gain of every 32 x 32 tile
+// of pairs, then of those), apply (the swap and the cheap updates), rows (the
+// six E rows).  All of them return at once when the search has stopped,
 // so the host enqueues max_swaps steps without waiting for any of them.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -325,49 +325,75 @@ __global__ void __launch_bounds__(256) perm_gains_kernel(const uint32_t* __restr
 // ---------------------------------------------------------------------------
 
 // The best swap: largest positive gain, then smallest a * 2^15 + b, as one
-// 64-bit key (gain << 30 | (2^30 - 1 - (a << 15 | b))) maximised with one
-// atomic per block.  Blocks stride over the 32 x 32 tiles with tA <= tB.
+// 64-bit key (gain << 30 | (2^30 - 1 - (a << 15 | b))).  One block per 32 x 32
+// tile of slot pairs with tA <= tB (the others return at once), so every
+// block's loads are in flight together; each block writes its largest key
+// (0: none) to its slot of `tile_best` (upper-triangle order), and the last
+// block to finish (a counter, no waiting) reduces them into ctl->key and
+// resets the counter.
 __global__ void __launch_bounds__(256) perm_best_kernel(const uint32_t* __restrict__ E,
-                                                        int32_t cols, PermCtl* ctl) {
+                                                        int32_t cols,
+                                                        unsigned long long* __restrict__ tile_best,
+                                                        PermCtl* ctl) {
   if (ctl->done) return;
+  const int tA = blockIdx.y, tB = blockIdx.x, nt = gridDim.x;
+  if (tA > tB) return;
   __shared__ uint32_t T[32][33], U[32][33], dA[32], dB[32];
   __shared__ unsigned long long red[8];
+  __shared__ int last;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int nt = cols / 32;
+  const int64_t a0 = static_cast<int64_t>(tA) * 32, b0 = static_cast<int64_t>(tB) * 32;
+  for (int i = ty; i < 32; i += 8) {
+    T[i][tx] = E[(a0 + i) * cols + b0 + tx];
+    U[i][tx] = E[(b0 + i) * cols + a0 + tx];
+  }
+  if (threadIdx.x < 32) dA[tx] = E[(a0 + tx) * (cols + 1)];
+  else if (threadIdx.x < 64) dB[tx] = E[(b0 + tx) * (cols + 1)];
+  __syncthreads();
   unsigned long long best = 0;
-  for (int64_t tile = blockIdx.x; tile < static_cast<int64_t>(nt) * nt; tile += gridDim.x) {
-    const int tA = static_cast<int>(tile / nt), tB = static_cast<int>(tile % nt);
-    if (tA > tB) continue;   // uniform over the block
-    const int64_t a0 = static_cast<int64_t>(tA) * 32, b0 = static_cast<int64_t>(tB) * 32;
-    __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-      T[i][tx] = E[(a0 + i) * cols + b0 + tx];
-      U[i][tx] = E[(b0 + i) * cols + a0 + tx];
-    }
-    if (threadIdx.x < 32) dA[tx] = E[(a0 + tx) * (cols + 1)];
-    else if (threadIdx.x < 64) dB[tx] = E[(b0 + tx) * (cols + 1)];
-    __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-      const int64_t a = a0 + i, b = b0 + tx;
-      if (a < b && (a >> 2) != (b >> 2)) {
-        const int64_t g =
-            (static_cast<int64_t>(T[i][tx]) - dA[i]) + (static_cast<int64_t>(U[tx][i]) - dB[tx]);
-        if (g > 0) {
-          const unsigned long long key =
-              (static_cast<unsigned long long>(g) << kKeyIndexBits) |
-              (kKeyIndexMask - static_cast<unsigned long long>((a << 15) | b));
-          best = key > best ? key : best;
-        }
+  for (int i = ty; i < 32; i += 8) {
+    const int64_t a = a0 + i, b = b0 + tx;
+    if (a < b && (a >> 2) != (b >> 2)) {
+      const int64_t g =
+          (static_cast<int64_t>(T[i][tx]) - dA[i]) + (static_cast<int64_t>(U[tx][i]) - dB[tx]);
+      if (g > 0) {
+        const unsigned long long key =
+            (static_cast<unsigned long long>(g) << kKeyIndexBits) |
+            (kKeyIndexMask - static_cast<unsigned long long>((a << 15) | b));
+        best = key > best ? key : best;
       }
     }
   }
   best = warp_max_u64(best);
   if (tx == 0) red[ty] = best;
   __syncthreads();
+  const uint32_t n_up = static_cast<uint32_t>(nt) * (nt + 1) / 2;
   if (threadIdx.x == 0) {
     unsigned long long m = 0;
     for (int w = 0; w < 8; ++w) m = red[w] > m ? red[w] : m;
-    if (m != 0) atomicMax(&ctl->key, m);
+    // upper-triangle index of (tA, tB)
+    const int64_t idx = static_cast<int64_t>(tA) * nt - static_cast<int64_t>(tA) * (tA - 1) / 2 +
+                        (tB - tA);
+    tile_best[idx] = m;
+    __threadfence();
+    last = atomicAdd(&ctl->tiles_done, 1u) == n_up - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  unsigned long long m = 0;
+  for (uint32_t i = threadIdx.x; i < n_up; i += blockDim.x) {
+    const unsigned long long k = *reinterpret_cast<volatile const unsigned long long*>(tile_best + i);
+    m = k > m ? k : m;
+  }
+  m = warp_max_u64(m);
+  if (tx == 0) red[ty] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long k = 0;
+    for (int w = 0; w < 8; ++w) k = red[w] > k ? red[w] : k;
+    ctl->key = k;
+    ctl->tiles_done = 0;
   }
 }
 
@@ -454,7 +480,6 @@ __global__ void __launch_bounds__(256) perm_rows_kernel(const uint32_t* __restri
                                                         PermCtl* ctl) {
   if (ctl->done) return;
   const int a = ctl->rec_a, b = ctl->rec_b;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) ctl->key = 0;
   // the i-th group-mate: i < 3 in a's group, i >= 3 in b's, skipping a and b
   auto mate = [&](int i) {
     const int s = i < 3 ? a : b, j = i < 3 ? i : i - 3;
@@ -593,6 +618,7 @@ struct Workspace {
   uint32_t* E;
   uint32_t* S;
   uint32_t* V;
+  unsigned long long* tile_best;
   PermCtl* ctl;
   uint32_t* seen;
 };
@@ -606,6 +632,8 @@ Workspace carve(void* ws, int64_t rows, int64_t cols) {
   p += round_up(rows * cols * 4, 256);
   w.V = reinterpret_cast<uint32_t*>(p);
   p += round_up(rows * cols * 4, 256);
+  w.tile_best = reinterpret_cast<unsigned long long*>(p);
+  p += round_up((cols / 32) * (cols / 32 + 1) / 2 * 8, 256);
   w.ctl = reinterpret_cast<PermCtl*>(p);
   p += round_up(static_cast<int64_t>(sizeof(PermCtl)), 256);
   w.seen = reinterpret_cast<uint32_t*>(p);
@@ -643,6 +671,7 @@ cudaError_t prepare_table(const Device& d, const uint16_t* W, int64_t rows, int6
 
 int64_t perm_workspace_bytes(int64_t rows, int64_t cols) {
   return round_up(cols * cols * 4, 256) + 2 * round_up(rows * cols * 4, 256) +
+         round_up((cols / 32) * (cols / 32 + 1) / 2 * 8, 256) +
          round_up(static_cast<int64_t>(sizeof(PermCtl)), 256) + round_up(cols, 32) / 8;
 }
 
@@ -655,7 +684,7 @@ cudaError_t perm_search(const Device& d, const uint16_t* W, int64_t rows, int64_
   if (e != cudaSuccess) return e;
   const int32_t c = static_cast<int32_t>(cols);
   const int64_t nt = cols / 32;
-  const int best_blocks = blocks_for(nt * nt, 1, 16LL * d.num_sms);
+  const dim3 best_grid(static_cast<unsigned>(nt), static_cast<unsigned>(nt));
   const int apply_blocks = blocks_for(rows > cols ? rows : cols, 256, 1LL << 30);
   const int col_blocks = static_cast<int>((cols + 511) / 512);
   int64_t slices = (2LL * d.num_sms + col_blocks - 1) / col_blocks;
@@ -665,7 +694,7 @@ cudaError_t perm_search(const Device& d, const uint16_t* W, int64_t rows, int64_
   const int64_t rows_per_slice = (rows + slices - 1) / slices;
   slices = (rows + rows_per_slice - 1) / rows_per_slice;
   for (int32_t it = 0; it < max_swaps; ++it) {
-    perm_best_kernel<<<best_blocks, 256, 0, s>>>(w.E, c, w.ctl);
+    perm_best_kernel<<<best_grid, 256, 0, s>>>(w.E, c, w.tile_best, w.ctl);
     perm_apply_kernel<<<apply_blocks, 256, 0, s>>>(perm, w.S, w.V, w.E, rows, c, w.ctl, swaps_out,
                                                    gains_out);
     perm_rows_kernel<<<dim3(col_blocks, static_cast<unsigned>(slices)), 256, 0, s>>>(

@@ -162,7 +162,7 @@ def test_next_entry_points_validation(L):
 
 def test_permutation_entry_points_validation(L):
     ws = L.maskllm_perm_workspace_bytes(64, 128)
-    assert ws == 128 * 128 * 4 + 2 * 64 * 128 * 4 + 256 + 128 // 8
+    assert ws == 128 * 128 * 4 + 2 * 64 * 128 * 4 + 256 + 256 + 128 // 8   # 10 tiles: 80 B
     assert L.maskllm_perm_workspace_bytes(64, 48) == 0            # cols % 32
     assert L.maskllm_perm_workspace_bytes(64, 32768 + 32) == 0    # cols above 32768
     assert L.maskllm_perm_workspace_bytes((1 << 24) + 1, 32) == 0

@@ -208,3 +208,25 @@ def test_search_full_size_q_proj():
     assert np.array_equal(host(p), cur)
     assert (orc.perm_metric_fixed(Wb, cur, k) - orc.perm_metric_fixed(Wb, ident, k)
             == int(gains.sum()))
+
+
+def test_search_steps_are_the_best_of_fresh_gain_tables():
+    """A longer search (each slot's list of best swaps is carried from step to
+    step): every step's swap is the best pair of a gain table computed from
+    scratch for that step's permutation (the tables themselves match the
+    oracle above)."""
+    rows, cols, steps = 200, 512, 120
+    Wt = weights(rows, cols, 77)
+    p = start_perm(cols, 78)
+    cur = p.clone()
+    n, swaps, gains, _ = run_search(Wt, p, steps)
+    assert n == steps
+    upper = np.triu(np.ones((cols, cols), bool), 1)
+    for (a, b), g in zip(swaps, gains):
+        table, info, _ = mk.maskllm_perm_swap_gains(Wt, cur)
+        t = np.where(upper, host(table), np.iinfo(np.int64).min)
+        best = t.max()
+        assert g == best > 0
+        assert [a, b] == np.argwhere(t == best)[0].tolist()
+        cur[a], cur[b] = cur[b].clone(), cur[a].clone()
+    assert torch.equal(cur, p)
