@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -52,54 +53,110 @@ __device__ uint32_t g_spmm_error_word = 0;
 
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;   // tile of C; dense K per stage
+// A CTA pair computes one 256 x 256 tile of C: CTA rank r of the cluster owns
+// rows 128 r .. 128 r + 127 of the tile (its own A rows, its own accumulator
+// lanes) and holds rows 128 r .. 128 r + 127 of the tile's 256 B rows.
+constexpr int kPairM = 256, kBM = 128, kBN = 256, kBNHalf = 128;
+constexpr int kBK = 128;      // dense K per stage: four K = 32 MMAs
+constexpr int kHalfK = 64;    // dense K per copy box (one 128-byte row of B)
 constexpr int kStages = 4;
 constexpr int kThreads = 256;
-constexpr uint32_t kABytes = kBM * (kBK / 2) * 2;   // 8 KB of values per stage
-constexpr uint32_t kBBytes = kBN * kBK * 2;         // 32 KB of B per stage
-constexpr uint32_t kARowBytes = kBK;                // 32 compressed values
-constexpr uint32_t kBRowBytes = kBK * 2;            // 64 values
-constexpr int kMetaAhead = 8;                       // stages of metadata loaded ahead
-constexpr uint32_t kTmemCols = 512;                 // D: 0..255, metadata: 256 + 64 s
+constexpr uint32_t kABox = kBM * (kHalfK / 2) * 2;   // 8 KB: 128 rows x 32 values
+constexpr uint32_t kBBox = kBNHalf * kHalfK * 2;     // 16 KB: 128 rows x 64 values
+constexpr uint32_t kAStage = 2 * kABox, kBStage = 2 * kBBox;
+constexpr uint32_t kARowBytes = 64, kBRowBytes = 128;
+constexpr uint32_t kMetaBlock = 128 * 16;            // 16 bytes per tensor-memory lane
+constexpr uint32_t kMetaStage = 2 * kMetaBlock;
+constexpr int kMetaAhead = 4;                        // stages of metadata words in registers
+constexpr uint32_t kTmemCols = 512;                  // D: 0..255, metadata: 256 + 128 p + 64 h
 constexpr uint32_t kMetaCol0 = 256;
+constexpr uint32_t kOutBox = kBM * 32 * 4;           // 16 KB: 128 rows x 32 fp32
 
 struct SmemLayout {
   static constexpr uint32_t kA = 0;
-  static constexpr uint32_t kB = kStages * kABytes;
-  static constexpr uint32_t kBar = kB + kStages * kBBytes;
-  // tma_full[s], meta_full[s], empty[s], done
-  static constexpr uint32_t kTmemSlot = kBar + (3 * kStages + 1) * 8;
+  static constexpr uint32_t kB = kStages * kAStage;
+  static constexpr uint32_t kMeta = kB + kStages * kBStage;
+  static constexpr uint32_t kBar = kMeta + kStages * kMetaStage;
+  // full[s], empty[s], done
+  static constexpr int kNumBars = 2 * kStages + 1;
+  static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kBytes = kAbort + 4 + 1024;   // + alignment slack
 };
+static_assert((kBN / 32) * kOutBox <= SmemLayout::kMeta, "C staging fits in the tile stages");
+
+// Arrivals on rank 0's full[s] per stage: its own expect-tx arrival, rank 1's
+// forwarded "copies landed", and one per metadata warp of both CTAs.
+constexpr uint32_t kFullArrivalsRank0 = 1 + 1 + 8;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address).
+// Default semantics: a cluster-scope release would also wait for this
+// thread's global loads still in flight (the metadata prefetch).  What the
+// arrivals publish is ordered before them by fence.proxy.async (metadata in
+// shared memory) or was observed complete on a barrier (copies).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                            int32_t y, uint64_t* bar) {
+                                            int32_t y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
 
-// Shared-memory matrix descriptor of a K-major swizzled tile: start address,
-// stride between 8-row groups, the fixed field value 1 at bit 46 and the
-// swizzle mode in bits 61-63 (2: 128-byte rows, 4: 64-byte rows).  The
-// leading byte offset is unused: one MMA's K extent lies inside a swizzle
-// row.  Tile bases are aligned to the swizzle pattern (8 rows).
-__device__ __forceinline__ uint64_t smem_desc_sw(uint32_t saddr, uint32_t group_stride,
-                                                 uint32_t mode) {
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y,
+                                             uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile: start address, leading
+// (K-direction) and stride (8-row group) byte offsets, the fixed field value
+// 1 at bit 46 and the swizzle mode in bits 61-63 (0: none, 2: 128-byte rows,
+// 4: 64-byte rows).  In a swizzled tile one MMA's K extent lies inside a
+// swizzle row (the leading offset is unused) and the MMA's K offset is added
+// to the start address; tile bases are aligned to the swizzle pattern.  In
+// the pair instructions the same descriptor addresses the same offset in both
+// CTAs.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lead, uint32_t stride,
+                                              uint32_t mode) {
   return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
-         (static_cast<uint64_t>((group_stride >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+         (static_cast<uint64_t>((lead >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((stride >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
          (static_cast<uint64_t>(mode) << 61);
 }
-constexpr uint32_t kSwizzle128 = 2, kSwizzle64 = 4;
+constexpr uint32_t kSwizzleNone = 0, kSwizzle128 = 2, kSwizzle64 = 4;
 
 // Instruction descriptor: sparse (bit 2) with selector `sel`, fp32 D, bf16 A
-// and B, both K-major, N = 256, M = 128.
+// and B, both K-major, N = 256, M = 256 (the pair's rows).
 __host__ __device__ constexpr uint32_t idesc_sparse(uint32_t sel) {
   return (sel & 3u) | (1u << 2) | (1u << 4) | (1u << 7) | (1u << 10) |
-         ((static_cast<uint32_t>(kBN) >> 3) << 17) | ((static_cast<uint32_t>(kBM) >> 4) << 24);
+         ((static_cast<uint32_t>(kBN) >> 3) << 17) |
+         ((static_cast<uint32_t>(kPairM) >> 4) << 24);
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -109,52 +166,72 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void mma_sparse(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t meta_tmem, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void mma_sparse_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                uint64_t b_desc, uint32_t meta_tmem,
+                                                uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
-      "tcgen05.mma.sp.cta_group::1.kind::f16 [%0], %1, %2, [%3], %4, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.sp.cta_group::2.kind::f16 [%0], %1, %2, [%3], %4, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(meta_tmem), "r"(idesc), "r"(acc)
       : "memory");
 }
 
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
+// Shared memory -> tensor memory, 128 lanes x 128 bits, in both CTAs of the
+// pair (each from its own shared memory into its own tensor memory).  Issued
+// by the MMA thread, it is performed in order with that thread's MMAs.
+__device__ __forceinline__ void tmem_copy_pair(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
 }
 
-__device__ __forceinline__ void raise(volatile int* abort_flag) {
+// Arrives once on the barrier at the same offset in both CTAs of the pair
+// when every earlier pair operation of this thread has completed.
+__device__ __forceinline__ void mma_commit_pair_both(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+// Raises this CTA's and the peer's abort flags and the device error word.
+__device__ __forceinline__ void raise(volatile int* abort_flag, uint32_t peer) {
   *abort_flag = 1;
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(
+                   map_to_rank(smem_u32(const_cast<int*>(abort_flag)), peer)),
+               "r"(1)
+               : "memory");
   atomicOr(&g_spmm_error_word, 1u);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     spmm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                const uint32_t* __restrict__ meta, float* __restrict__ C, int32_t M, int32_t N,
-                int32_t K, uint64_t wait_ns) {
+                const __grid_constant__ CUtensorMap map_c, const uint32_t* __restrict__ meta,
+                float* __restrict__ C, int32_t M, int32_t N, int32_t K, int32_t tma_store,
+                uint64_t wait_ns) {
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte aligned base
+  // 1024-byte aligned base (the same offset in every CTA)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::kBar);
-  uint64_t* tma_full = bars;
-  uint64_t* meta_full = bars + kStages;
-  uint64_t* empty = bars + 2 * kStages;
-  uint64_t* done = bars + 3 * kStages;
+  uint64_t* full = bars;              // rank 0: the stage is ready for the pair's MMAs
+                                      // rank 1: this CTA's copies of the stage landed
+  uint64_t* empty = bars + kStages;   // both: the pair's MMAs are done with the stage
+  uint64_t* done = empty + kStages;   // both: every MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::kAbort);
   const uint32_t sA = smem_u32(smem + SmemLayout::kA);
   const uint32_t sB = smem_u32(smem + SmemLayout::kB);
+  const uint32_t sMeta = smem_u32(smem + SmemLayout::kMeta);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
-  const int nk = (K + kBK - 1) / kBK;   // K % 32 == 0; a half stage reads zeros
-  const int kw = K / 32;                // metadata words per row
+  const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
+  const int m0 = (blockIdx.x >> 1) * kPairM + static_cast<int>(rank) * kBM;   // this CTA's rows
+  const int n0 = blockIdx.y * kBN;
+  const int nk = (K + kBK - 1) / kBK;
+  const int kw = K / 32;   // K % 32 == 0: metadata words per row
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&tma_full[s], 1);
-      mbar_init(&meta_full[s], 4);
+      mbar_init(&full[s], rank == 0 ? kFullArrivalsRank0 : 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(done, 1);
@@ -162,68 +239,94 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+    // the pair allocates together: one warp of each CTA, the same columns
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  // both CTAs' barriers are initialised before either touches the other's
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---- TMA producer ----
+    // ---- copies of this CTA's tiles (each CTA's own copy engine) ----
     int issued = 0;
     if (lane == 0) {
       for (int kt = 0; kt < nk; ++kt) {
         const int s = kt % kStages;
         if (kt >= kStages &&
             !mbar_wait_bounded(&empty[s], ((kt / kStages) - 1) & 1, wait_ns, abort_flag)) {
-          raise(abort_flag);
+          raise(abort_flag, peer);
           break;
         }
-        mbar_arrive_expect_tx(&tma_full[s], kABytes + kBBytes);
-        tma_load_2d(sA + s * kABytes, &map_a, kt * (kBK / 2), m0, &tma_full[s]);
-        tma_load_2d(sB + s * kBBytes, &map_b, kt * kBK, n0, &tma_full[s]);
+        // one or two 64-deep halves (K % 32 == 0; a half past K reads zeros)
+        const int nbox = (K - kt * kBK > kHalfK) ? 2 : 1;
+        const uint32_t bar = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nbox) * (kABox + kBBox));
+        for (int h = 0; h < nbox; ++h) {
+          tma_load_2d(sA + s * kAStage + h * kABox, &map_a, kt * (kBK / 2) + h * (kHalfK / 2),
+                      m0, bar);
+          tma_load_2d(sB + s * kBStage + h * kBBox, &map_b, kt * kBK + h * kHalfK,
+                      n0 + static_cast<int>(rank) * kBNHalf, bar);
+        }
         issued = kt + 1;
       }
       if (*abort_flag) {
-        // wait (bounded) for the copies still landing in shared memory
+        // wait (bounded) for the copies still landing in this CTA
         for (int kt = issued > kStages ? issued - kStages : 0; kt < issued; ++kt) {
           int never = 0;
-          mbar_wait_bounded(&tma_full[kt % kStages], (kt / kStages) & 1, wait_ns, &never);
+          mbar_wait_bounded(&full[kt % kStages], (kt / kStages) & 1, wait_ns, &never);
         }
       }
     }
-  } else if (warp == 1) {
-    // ---- MMA issuer ----
+  } else if (warp == 2 && rank == 1) {
+    // ---- forwards "copies landed" to rank 0's stage barrier ----
     if (lane == 0) {
       for (int kt = 0; kt < nk; ++kt) {
         const int s = kt % kStages;
-        const uint32_t ph = (kt / kStages) & 1;
-        if (!mbar_wait_bounded(&tma_full[s], ph, wait_ns, abort_flag) ||
-            !mbar_wait_bounded(&meta_full[s], ph, wait_ns, abort_flag)) {
-          raise(abort_flag);
+        if (!mbar_wait_bounded(&full[s], (kt / kStages) & 1, wait_ns, abort_flag)) {
+          raise(abort_flag, peer);
+          break;
+        }
+        mbar_arrive_remote(map_to_rank(smem_u32(&full[s]), 0));
+      }
+    }
+  } else if (warp == 1 && rank == 0) {
+    // ---- the pair's MMAs ----
+    if (lane == 0) {
+      for (int kt = 0; kt < nk; ++kt) {
+        const int s = kt % kStages;
+        if (!mbar_wait_bounded(&full[s], (kt / kStages) & 1, wait_ns, abort_flag)) {
+          raise(abort_flag, peer);
           break;
         }
         tc_fence_after();
-        const uint32_t a = sA + s * kABytes, b = sB + s * kBBytes;
-        const uint32_t meta_t = tmem + kMetaCol0 + 64u * s;
-        // the second K = 32 block of the last stage is absent when K % 64 == 32
-        const int nkb = (2 * kt + 1 < kw) ? 2 : 1;
+        // the stage's metadata into tensor memory: two 4-column blocks at
+        // 64-aligned columns (K blocks 0, 1 and 2, 3), alternating by stage
+        const uint32_t meta_t = tmem + kMetaCol0 + 128u * (kt & 1);
+        const uint32_t ms = sMeta + s * kMetaStage;
+        tmem_copy_pair(meta_t, smem_desc(ms, 2048, 128, kSwizzleNone));
+        tmem_copy_pair(meta_t + 64, smem_desc(ms + kMetaBlock, 2048, 128, kSwizzleNone));
+        const uint32_t a = sA + s * kAStage, b = sB + s * kBStage;
+        const int nkb = min(4, kw - 4 * kt);
         for (int kb = 0; kb < nkb; ++kb) {
-          // K block kb: 16 compressed values (32 bytes) of A, 32 values (64
-          // bytes) of B into the swizzle row
-          const uint64_t ad = smem_desc_sw(a + kb * 32, 8 * kARowBytes, kSwizzle64);
-          const uint64_t bd = smem_desc_sw(b + kb * 64, 8 * kBRowBytes, kSwizzle128);
-          mma_sparse(tmem, ad, bd, meta_t, idesc_sparse(kb), (kt | kb) != 0);
+          // K block kb: half kb / 2, position kb % 2 in the swizzle row (16
+          // compressed values = 32 bytes of A, 32 values = 64 bytes of B)
+          const int h = kb >> 1, sub = kb & 1;
+          const uint64_t ad =
+              smem_desc(a + h * kABox + sub * 32, 0, 8 * kARowBytes, kSwizzle64);
+          const uint64_t bd =
+              smem_desc(b + h * kBBox + sub * 64, 0, 8 * kBRowBytes, kSwizzle128);
+          mma_sparse_pair(tmem, ad, bd, meta_t + 64u * h, idesc_sparse(sub), (kt | kb) != 0);
         }
-        mma_commit(&empty[s]);
+        mma_commit_pair_both(&empty[s]);
       }
       // completes when every MMA issued above has (also after an abort)
-      mma_commit(done);
+      mma_commit_pair_both(done);
     }
   } else if (warp >= 4) {
     // ---- metadata, then epilogue; thread q owns tensor-memory lane q ----
@@ -233,20 +336,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ra = m0 + 16 * blk + (i & 7), rb = ra + 8;
     const bool hi = i >= 8;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quad) << 16);
-    // the two words of stage kt for this lane: low 16 bits from row ra, high
-    // 16 bits from row rb, the k 0..15 or k 16..31 halves
-    auto fetch = [&](int kt, uint32_t (&w)[2]) {
+    // The sparse MMA reads the metadata of a 16-row block interleaved: lane
+    // i < 8 holds the k 0..15 halves of rows i (low 16 bits) and i + 8
+    // (high), lane 8 + i the k 16..31 halves of the same rows.  The four
+    // words of stage kt for this lane, one per K = 32 block:
+    auto fetch = [&](int kt, uint32_t (&w)[4]) {
 #pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-        const int word = 2 * kt + kb;
+      for (int kb = 0; kb < 4; ++kb) {
+        const int word = 4 * kt + kb;
         const uint32_t wa = (ra < M && word < kw) ? __ldg(meta + static_cast<int64_t>(ra) * kw + word) : 0u;
         const uint32_t wb = (rb < M && word < kw) ? __ldg(meta + static_cast<int64_t>(rb) * kw + word) : 0u;
         w[kb] = hi ? __byte_perm(wa, wb, 0x7632) : __byte_perm(wa, wb, 0x5410);
       }
     };
-    uint32_t ring[kMetaAhead][2];
+    uint32_t ring[kMetaAhead][4];
 #pragma unroll
     for (int u = 0; u < kMetaAhead; ++u) fetch(u, ring[u]);
+    const uint32_t full0 = map_to_rank(smem_u32(&full[0]), 0);
     bool ok = true;
     for (int kt0 = 0; kt0 < nk && ok; kt0 += kMetaAhead) {
 #pragma unroll
@@ -258,30 +364,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait_bounded(&empty[s], ((kt / kStages) - 1) & 1, wait_ns, abort_flag);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) {
-            if (lane == 0) raise(abort_flag);
+            if (lane == 0) raise(abort_flag, peer);
             break;
           }
-          tc_fence_after();
         }
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(
-                         lane_base + kMetaCol0 + 64u * s),
-                     "r"(ring[u][0]), "r"(ring[u][1])
-                     : "memory");
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
+        // lane q's 16-byte rows of the stage's two metadata blocks
+        uint8_t* ms = smem + SmemLayout::kMeta + s * kMetaStage + 16 * q;
+        sts128(ms, make_uint4(ring[u][0], ring[u][1], 0u, 0u));
+        sts128(ms + kMetaBlock, make_uint4(ring[u][2], ring[u][3], 0u, 0u));
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&meta_full[s]);
+        if (lane == 0) mbar_arrive_remote(full0 + 8u * s);
         fetch(kt + kMetaAhead, ring[u]);   // zeros past the end
       }
     }
-    // epilogue
+    // epilogue: tensor memory -> registers -> C
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(done, 0, wait_ns, abort_flag));
-    if (!ok && lane == 0) raise(abort_flag);
+    if (!ok && lane == 0) raise(abort_flag, peer);
+    const int m = m0 + q;
     if (ok) {
       tc_fence_after();
-      const int m = m0 + q;
       float* crow = C + static_cast<int64_t>(m) * N;
-      const bool vec = (N % 4) == 0;
 #pragma unroll 1
       for (int c0 = 0; c0 < kBN; c0 += 32) {
         uint32_t v[32];
@@ -296,33 +399,49 @@ __global__ void __launch_bounds__(kThreads, 1)
               "=r"(v[31])
             : "r"(lane_base + static_cast<uint32_t>(c0)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (m < M) {
+        if (tma_store) {
+          // staged for a bulk store: box c0 / 32 (128 rows x 128 bytes,
+          // 128-byte swizzle: 16-byte chunk j of row q at chunk j ^ (q % 8))
+          uint8_t* row = smem + (c0 / 32) * kOutBox + 128 * q;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            sts128(row + 16 * (j ^ (q & 7)),
+                   make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        } else if (m < M) {
           const int n = n0 + c0;
-          if (vec && n + 32 <= N) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              __stcs(reinterpret_cast<float4*>(crow + n + j),
-                     make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                 __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (n + j < N) crow[n + j] = __uint_as_float(v[j]);
-          }
+          for (int j = 0; j < 32; ++j)
+            if (n + j < N) crow[n + j] = __uint_as_float(v[j]);
         }
       }
     }
+    if (tma_store) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      // every epilogue warp arrives here, whatever happened above
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (q == 0 && !*abort_flag && m0 < M) {
+        for (int c = 0; c < kBN / 32 && n0 + 32 * c < N; ++c)
+          tma_store_2d(&map_c, n0 + 32 * c, m0, smem_u32(smem + c * kOutBox));
+        bulk_commit();
+        bulk_wait_all();
+      }
+    }
+  }
+  if (warp == 1 && rank == 0 && *abort_flag) {
+    // every MMA issued has completed (bounded wait) before either CTA's
+    // tensor memory or shared memory goes
+    int never = 0;
+    mbar_wait_bounded(done, 0, wait_ns, &never);
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  // neither CTA leaves while the other may still reach its shared or tensor
+  // memory
+  cluster_sync();
   if (warp == 1) {
-    // every MMA issued has completed (bounded wait) before the memory goes
-    if (*abort_flag) {
-      int never = 0;
-      mbar_wait_bounded(done, 0, wait_ns, &never);
-    }
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
   }
@@ -344,18 +463,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over [rows, cols] row-major with a box of box_cols
-// values (box_cols * 2 bytes = the swizzle row) x box_rows rows.
-bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, uint32_t box_cols,
-              uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+// 2-D tensor map over [rows, cols] row-major (bf16 or fp32) with a box of
+// box_cols values (box_cols x element size = the swizzle row) x box_rows rows.
+bool make_map(CUtensorMap* map, CUtensorMapDataType type, uint32_t elem_bytes, const void* base,
+              int64_t rows, int64_t cols, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle swizzle) {
   const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem_bytes};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t elem[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(map, type, 2, const_cast<void*>(base), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -363,18 +483,29 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, ui
 
 cudaError_t spmm(const Device&, const uint16_t* values, const uint32_t* meta, int64_t M, int64_t K,
                  const uint16_t* B, int64_t N, float* C, uint64_t wait_ns, cudaStream_t s) {
-  CUtensorMap map_a, map_b;
-  if (!make_map(&map_a, values, M, K / 2, kBK / 2, kBM, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&map_b, B, N, K, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+  CUtensorMap map_a, map_b, map_c;
+  if (!make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, values, M, K / 2, kHalfK / 2, kBM,
+                CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, kHalfK, kBNHalf,
+                CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  // C leaves through bulk stores when its rows are 16-byte multiples on a
+  // 16-byte aligned base; otherwise each thread stores its row directly
+  std::memset(&map_c, 0, sizeof(map_c));
+  const bool tma_store =
+      (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) % 16) == 0 &&
+      make_map(&map_c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, 32, kBM,
+               CU_TENSOR_MAP_SWIZZLE_128B);
   const uint32_t smem = SmemLayout::kBytes;
   cudaError_t e =
       cudaFuncSetAttribute(spmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>((N + kBN - 1) / kBN), static_cast<unsigned>((M + kBM - 1) / kBM));
-  spmm_kernel<<<grid, kThreads, smem, s>>>(map_a, map_b, meta, C, static_cast<int32_t>(M),
+  // x: two CTAs (one cluster) per 256 rows of C; y: 256 columns of C
+  const dim3 grid(static_cast<unsigned>(2 * ((M + kPairM - 1) / kPairM)),
+                  static_cast<unsigned>((N + kBN - 1) / kBN));
+  spmm_kernel<<<grid, kThreads, smem, s>>>(map_a, map_b, map_c, meta, C, static_cast<int32_t>(M),
                                            static_cast<int32_t>(N), static_cast<int32_t>(K),
-                                           wait_ns);
+                                           tma_store ? 1 : 0, wait_ns);
   return cudaGetLastError();
 }
 
