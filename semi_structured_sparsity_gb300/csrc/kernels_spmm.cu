@@ -60,7 +60,7 @@ constexpr int kPairM = 256, kBM = 128, kBN = 256, kBNHalf = 128;
 constexpr int kBK = 128;      // dense K per stage: four K = 32 MMAs
 constexpr int kHalfK = 64;    // dense K per copy box (one 128-byte row of B)
 constexpr int kStages = 4;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr uint32_t kABox = kBM * (kHalfK / 2) * 2;   // 8 KB: 128 rows x 32 values
 constexpr uint32_t kBBox = kBNHalf * kHalfK * 2;     // 16 KB: 128 rows x 64 values
 constexpr uint32_t kAStage = 2 * kABox, kBStage = 2 * kBBox;
@@ -229,6 +229,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int nk = (K + kBK - 1) / kBK;
   const int kw = K / 32;   // K % 32 == 0: metadata words per row
 
+  // copies of stage kt of this CTA's tiles: one or two 64-deep halves
+  // (K % 32 == 0; a half past K reads zeros), counted on full[kt % kStages]
+  auto issue_stage = [&](int kt) {
+    const int s = kt % kStages;
+    const int nbox = (K - kt * kBK > kHalfK) ? 2 : 1;
+    const uint32_t bar = smem_u32(&full[s]);
+    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nbox) * (kABox + kBBox));
+    for (int h = 0; h < nbox; ++h) {
+      tma_load_2d(sA + s * kAStage + h * kABox, &map_a, kt * (kBK / 2) + h * (kHalfK / 2), m0,
+                  bar);
+      tma_load_2d(sB + s * kBStage + h * kBBox, &map_b, kt * kBK + h * kHalfK,
+                  n0 + static_cast<int>(rank) * kBNHalf, bar);
+    }
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], rank == 0 ? kFullArrivalsRank0 : 1);
@@ -263,16 +277,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           raise(abort_flag, peer);
           break;
         }
-        // one or two 64-deep halves (K % 32 == 0; a half past K reads zeros)
-        const int nbox = (K - kt * kBK > kHalfK) ? 2 : 1;
-        const uint32_t bar = smem_u32(&full[s]);
-        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nbox) * (kABox + kBBox));
-        for (int h = 0; h < nbox; ++h) {
-          tma_load_2d(sA + s * kAStage + h * kABox, &map_a, kt * (kBK / 2) + h * (kHalfK / 2),
-                      m0, bar);
-          tma_load_2d(sB + s * kBStage + h * kBBox, &map_b, kt * kBK + h * kHalfK,
-                      n0 + static_cast<int>(rank) * kBNHalf, bar);
-        }
+        issue_stage(kt);
         issued = kt + 1;
       }
       if (*abort_flag) {
@@ -329,8 +334,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mma_commit_pair_both(done);
     }
   } else if (warp >= 4) {
-    // ---- metadata, then epilogue; thread q owns tensor-memory lane q ----
-    const int q = threadIdx.x - 128;
+    // ---- warps 4-7: metadata, then the epilogue of columns 0..127;
+    //      warps 8-11: the epilogue of columns 128..255.  Thread q of a
+    //      group owns tensor-memory lane q. ----
+    const int g = (warp - 4) >> 2;
+    const int q = (threadIdx.x - 128) & 127;
     const int quad = warp & 3;   // lanes 32 quad .. 32 quad + 31 (== q >> 5)
     const int blk = q >> 4, i = q & 15;
     const int ra = m0 + 16 * blk + (i & 7), rb = ra + 8;
@@ -349,12 +357,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         w[kb] = hi ? __byte_perm(wa, wb, 0x7632) : __byte_perm(wa, wb, 0x5410);
       }
     };
-    uint32_t ring[kMetaAhead][4];
+    uint32_t ring[kMetaAhead][4] = {};
+    if (g == 0) {
 #pragma unroll
-    for (int u = 0; u < kMetaAhead; ++u) fetch(u, ring[u]);
+      for (int u = 0; u < kMetaAhead; ++u) fetch(u, ring[u]);
+    }
     const uint32_t full0 = map_to_rank(smem_u32(&full[0]), 0);
     bool ok = true;
-    for (int kt0 = 0; kt0 < nk && ok; kt0 += kMetaAhead) {
+    for (int kt0 = 0; kt0 < nk && ok && g == 0; kt0 += kMetaAhead) {
 #pragma unroll
       for (int u = 0; u < kMetaAhead; ++u) {
         const int kt = kt0 + u;
@@ -378,15 +388,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fetch(kt + kMetaAhead, ring[u]);   // zeros past the end
       }
     }
-    // epilogue: tensor memory -> registers -> C
+    // epilogue: tensor memory -> registers -> C, 32 columns at a time
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(done, 0, wait_ns, abort_flag));
     if (!ok && lane == 0) raise(abort_flag, peer);
+    if (ok) tc_fence_after();
     const int m = m0 + q;
-    if (ok) {
-      tc_fence_after();
-      float* crow = C + static_cast<int64_t>(m) * N;
+    float* crow = C + static_cast<int64_t>(m) * N;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
+    for (int cb = 0; cb < kBN / 64; ++cb) {
+      const int c = (kBN / 64) * g + cb;   // box of columns 32 c .. 32 c + 31
+      if (ok) {
         uint32_t v[32];
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
@@ -397,35 +408,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
               "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
               "=r"(v[31])
-            : "r"(lane_base + static_cast<uint32_t>(c0)));
+            : "r"(lane_base + static_cast<uint32_t>(32 * c)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         if (tma_store) {
-          // staged for a bulk store: box c0 / 32 (128 rows x 128 bytes,
-          // 128-byte swizzle: 16-byte chunk j of row q at chunk j ^ (q % 8))
-          uint8_t* row = smem + (c0 / 32) * kOutBox + 128 * q;
+          // staged for a bulk store: box c (128 rows x 128 bytes, 128-byte
+          // swizzle: 16-byte chunk j of row q at chunk j ^ (q % 8))
+          uint8_t* row = smem + c * kOutBox + 128 * q;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             sts128(row + 16 * (j ^ (q & 7)),
                    make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
         } else if (m < M) {
-          const int n = n0 + c0;
+          const int n = n0 + 32 * c;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (n + j < N) crow[n + j] = __uint_as_float(v[j]);
         }
       }
-    }
-    if (tma_store) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      // every epilogue warp arrives here, whatever happened above
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (q == 0 && !*abort_flag && m0 < M) {
-        for (int c = 0; c < kBN / 32 && n0 + 32 * c < N; ++c)
+      if (tma_store) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        // every warp of the group arrives here, whatever happened above;
+        // the box leaves as soon as it is staged
+        if (g == 0)
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+        else
+          asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (q == 0 && !*abort_flag && m0 < M && n0 + 32 * c < N)
           tma_store_2d(&map_c, n0 + 32 * c, m0, smem_u32(smem + c * kOutBox));
-        bulk_commit();
-        bulk_wait_all();
       }
+    }
+    if (tma_store && q == 0) {
+      // the stores have read shared memory before the CTA may leave; their
+      // writes to C complete on their own
+      bulk_commit();
+      bulk_wait_reads();
     }
   }
   if (warp == 1 && rank == 0 && *abort_flag) {
