@@ -10,31 +10,36 @@
 // second operand and skips the zeros: twice the math throughput of the dense
 // product).
 //
-// One CTA per 128 x 256 tile of C (tcgen05.mma.sp, kind::f16, cta_group::1:
-// M = 128, N = 256, K = 32 per instruction; the fp32 accumulator is 256
-// columns of tensor memory).  K advances 64 per pipeline stage (two MMAs);
-// four stages of shared memory.
-//   warp 0     TMA: per stage one box of A values (128 rows x 32 values, 64
-//              bytes a row, 64-byte swizzle) and one of B (256 rows x 64
-//              values, 128 bytes a row, 128-byte swizzle), the K-major
-//              swizzled layouts the MMA reads (8-row groups 512 / 1024 bytes
-//              apart; the MMA's K offset inside the swizzle row is added to
-//              the descriptor's start address).
-//   warp 1     allocates tensor memory; one thread issues the MMAs, commits
-//              each stage's MMAs to the stage's "empty" barrier and the last
-//              ones to "done".
+// A cluster of two CTAs (one per SM) computes a 256 x 256 tile of C with the
+// pair form of the sparse MMA (tcgen05.mma.sp.cta_group::2, kind::f16: M =
+// 256, 128 rows in each SM; N = 256, each SM holding 128 rows of B; K = 32 per
+// instruction; the fp32 accumulator is 256 columns of each SM's tensor
+// memory).  Per SM and MMA the tensor core reads 4 KB of A and 8 KB of B from
+// shared memory, against 4 + 16 KB for a single-SM M = 128 tile.  K advances
+// 128 per stage (four MMAs); four stages.
+//   warp 0     (both CTAs) copies its own tiles per stage: two boxes of A
+//              values (128 rows x 32 values, 64-byte rows, 64-byte swizzle)
+//              and two of B (128 rows x 64 values, 128-byte rows, 128-byte
+//              swizzle), the K-major swizzled layouts the MMA reads.
+//   warp 1     allocates the pair's tensor memory (both CTAs together); in
+//              rank 0 one thread waits for each stage, copies the stage's
+//              metadata into tensor memory (tcgen05.cp, performed in order
+//              with its MMAs), issues the four MMAs and commits them to the
+//              stage's "empty" barrier in both CTAs, the last to "done".
+//   warp 2     (rank 1) forwards "this CTA's copies landed" to rank 0.
 //   warps 4-7  one tensor-memory lane per thread.  Per stage they write the
-//              stage's metadata into tensor memory (two 32-bit columns at a
-//              64-column-aligned base; the MMA's selector field picks the
-//              column of its K = 32 block).  The sparse MMA reads the
-//              metadata of a 16-row block interleaved: lane i < 8 holds the
-//              k 0..15 halves of rows i (low 16 bits) and i + 8 (high), lane
-//              8 + i the k 16..31 halves of the same rows -- built here from
-//              the plain row-major codes with two byte permutes.  Then the
-//              epilogue: tensor memory -> registers -> C (fp32, row-major).
-// Every wait is bounded (pipeline.cuh); on a timeout the CTA raises its abort
-// flag and the device error word, waits (bounded) for copies and MMAs in
-// flight, frees its tensor memory and returns.
+//              stage's metadata into shared memory in the order the sparse
+//              MMA reads it from tensor memory: per 16-row block lane i < 8
+//              holds the k 0..15 halves of rows i (low 16 bits) and i + 8
+//              (high), lane 8 + i the k 16..31 halves of the same rows --
+//              built from the plain row-major codes with two byte permutes.
+//   warps 4-11 the epilogue: tensor memory -> registers -> shared memory
+//              (32-column boxes, 128-byte swizzle) -> bulk tensor stores of
+//              C, each box sent as soon as it is staged (columns 0..127 by
+//              warps 4-7, 128..255 by warps 8-11).
+// Every wait is bounded (pipeline.cuh); on a timeout the CTA raises its own
+// and its peer's abort flag and the device error word, waits (bounded) for
+// copies and MMAs in flight, and the pair frees its tensor memory together.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
