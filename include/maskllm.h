@@ -297,7 +297,8 @@ maskllm_status maskllm_perm_search(const uint16_t* W, int64_t rows, int64_t cols
  *   C       out  fp32 [M, N] row-major
  * Products are exact in fp32; they are summed in fp32 on the tensor cores in
  * an order of their own.  M, N >= 1, K >= 32, K % 32 == 0, M, N < 2^31,
- * K < 2^31.  A bounded wait that gives up makes the next
+ * K < 2^31, N <= 65535 * 256.  C is written by bulk tensor stores when
+ * N % 4 == 0 and row by row otherwise.  A bounded wait that gives up makes the next
  * maskllm_device_status() return MASKLLM_ERR_TIMEOUT; MASKLLM_ERR_CUDA if the
  * driver cannot describe the operands to the copy engine. */
 maskllm_status maskllm_spmm(const uint16_t* values, const uint32_t* meta, int64_t M, int64_t K,

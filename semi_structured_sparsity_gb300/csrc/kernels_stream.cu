@@ -171,6 +171,14 @@ __device__ int64_t cta_first_unit(const StreamParams& p, int64_t b, int64_t G) {
   return d.unit_begin + u;
 }
 
+// The launch's chunk index of the first chunk of unit u (u may be the total).
+__device__ int64_t chunk_index(const StreamParams& p, int64_t u) {
+  int m = 0;
+  while (m + 1 < p.nmats && p.mats[m + 1].unit_begin <= u) ++m;
+  const MatDesc& d = p.mats[m];
+  return d.chunk_begin + (u - d.unit_begin) * (d.cpr > 0 ? d.cpr : 1);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -793,7 +801,9 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
   if (Op::kStaged && lane == 0) bulk_wait_all();
 }
 
-// Consumer warps: thread t owns GPT groups of every chunk.
+// Consumer warps: thread t owns GPT groups of every chunk.  The chunk in a
+// stage is the one the producer recorded there (held[s], written before its
+// arrival on full[s]); the consumers only count their chunks.
 template <class Op>
 __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64_t u1) {
   using Lay = Layout<Op>;
@@ -804,14 +814,12 @@ __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
   const float* tab = reinterpret_cast<const float*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
   uint64_t* empty = full + S;
+  const Chunk* held = reinterpret_cast<const Chunk*>(smem + Lay::kChunkOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kFlagOff);
 
-  ChunkIter it;
-  it.init(&p, u0, u1);
-  Chunk c;
-  int64_t n = 0;
+  const int64_t nchunks = chunk_index(p, u1) - chunk_index(p, u0);
   float acc[3] = {0.f, 0.f, 0.f};   // per-row quantities of this thread
-  while (it.next(c)) {
+  for (int64_t n = 0; n < nchunks; ++n) {
     const int s = static_cast<int>(n % S);
     const bool got = mbar_wait_bounded(&full[s], static_cast<uint32_t>((n / S) & 1), p.wait_ns,
                                        abort_flag);
@@ -819,6 +827,7 @@ __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
       if (lane == 0) raise_abort(abort_flag, 1u);
       break;
     }
+    const Chunk c = held[s];
     const MatDesc& d = p.mats[c.mat];
     uint8_t* st = stages + s * Op::kStageBytes;
     if (Op::kWarpWide)
@@ -840,7 +849,6 @@ __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
     if (Op::kStaged) fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    ++n;
   }
 }
 

@@ -726,7 +726,8 @@ extern "C" maskllm_status maskllm_spmm(const uint16_t* values, const uint32_t* m
   MK_TRY(maskllm::check_ptrs(ptrs, 4));
   if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return MASKLLM_ERR_SHAPE;
   const int64_t lim = (int64_t(1) << 31) - 1;
-  if (M > lim || N > lim || K > lim || (M + 127) / 128 > 65535) return MASKLLM_ERR_SHAPE;
+  // the grid holds one CTA pair per 256 rows of C in x and 256 columns in y
+  if (M > lim || N > lim || K > lim || (N + 255) / 256 > 65535) return MASKLLM_ERR_SHAPE;
   maskllm::Spans sp;
   sp.input(values, static_cast<uint64_t>(M) * static_cast<uint64_t>(K));
   sp.input(meta, static_cast<uint64_t>(M) * static_cast<uint64_t>(K) / 8);

@@ -201,6 +201,7 @@ def test_spmm_validation(L):
     assert L.maskllm_spmm(A, B, 128, 48, Cc, 256, D, None) == SHAPE       # K % 32
     assert L.maskllm_spmm(A, B, 0, 64, Cc, 256, D, None) == SHAPE
     assert L.maskllm_spmm(A, B, 128, 64, Cc, 0, D, None) == SHAPE
+    assert L.maskllm_spmm(A, B, 128, 64, Cc, 65535 * 256 + 1, D, None) == SHAPE   # grid y
     assert L.maskllm_spmm(A + 8, B, 128, 64, Cc, 256, D, None) == ALIGN
     assert L.maskllm_spmm(A, B, 128, 64, Cc, 256, Cc + 64, None) == ALIAS  # C over B
 

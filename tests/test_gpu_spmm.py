@@ -55,7 +55,11 @@ def to_gpu(vals, meta, Bb):
 
 
 @pytest.mark.parametrize("M,K,N", [(128, 64, 256), (200, 96, 300), (1, 32, 1), (257, 128, 5),
-                                   (384, 1024, 520), (130, 32, 257)])
+                                   (384, 1024, 520), (130, 32, 257),
+                                   # last 128-deep stage with one 64-deep half
+                                   # (K = 160) or three K = 32 blocks (K = 224);
+                                   # the second CTA of a pair holding one row
+                                   (129, 160, 256), (512, 224, 136), (385, 4096, 64)])
 def test_small_integers_bit_exact(M, K, N):
     vals, meta, Bb = operands(M, K, N, M + K + N, integers=True)
     C = mk.maskllm_spmm(*to_gpu(vals, meta, Bb))
@@ -71,6 +75,21 @@ def test_real_values_within_bound(M, K, N):
     want, S = orc.spmm(vals, meta, M, K, Bb)
     err = np.abs(C - want)
     assert (err <= RTOL_S * S + 1e-30).all(), float((err / (S + 1e-30)).max())
+
+
+def test_output_not_16_byte_aligned_is_rejected():
+    """Every pointer of the library starts on a 16-byte boundary; a C four
+    bytes off is refused before anything runs and left untouched."""
+    M, K, N = 300, 256, 256
+    vals, meta, Bb = operands(M, K, N, 11, integers=True)
+    v, m, b = to_gpu(vals, meta, Bb)
+    buf = torch.full((M * N + 1,), float("nan"), device="cuda")
+    C = buf[1:].view(M, N)
+    assert C.data_ptr() % 16 != 0
+    with pytest.raises(mk.MaskLLMError, match="ALIGNMENT"):
+        mk.maskllm_spmm(v, m, b, C=C)
+    assert torch.isnan(buf).all()
+    assert mk.maskllm_device_status() == 0
 
 
 def test_two_calls_in_a_row_and_output_overwritten():
