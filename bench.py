@@ -695,10 +695,58 @@ def oracle_step(wl, sample, step: int):
         orc.hard_compress(Wb, L)
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (x86 "model name"; on Arm the
+    implementer and part codes)."""
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return "implementer %s part %s" % (fields.get("CPU implementer", "?"), fields["CPU part"])
+    import platform
+    return platform.machine()
+
+
+def oracle_step_sharded(wl, sample, step: int, threads: int):
+    """One oracle pass over the sample with every matrix split into `threads`
+    row shards, one task per shard on a pool of `threads` threads (the
+    oracle's compiled calls release the interpreter lock; row_begin keeps each
+    shard's noise counters those of the whole matrix)."""
+    import oracle as orc
+    from concurrent.futures import ThreadPoolExecutor
+    orc.gumbel_noise(0, 0, 0, 0, 1)   # the oracle's table, built once before the threads
+    tasks = []
+    for Wb, L, Gb, tid in sample:
+        rows = Wb.shape[0]
+        for i in range(threads):
+            a, b = rows * i // threads, rows * (i + 1) // threads
+            if b > a:
+                tasks.append((Wb[a:b], L[a:b], Gb[a:b], tid, a))
+
+    def run(task):
+        Wb, L, Gb, tid, r0 = task
+        orc.prior_init(Wb, wl.prior_scale or 1.0)
+        orc.forward(Wb, L, wl.tau, wl.kappa, 0, step, tid, row_begin=r0)
+        orc.backward(Wb, L, Gb, wl.tau, wl.kappa, 0, step, tid, row_begin=r0)
+        orc.hard_compress(Wb, L)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run, tasks))
+
+
 def cpu_baseline(wl, target_seconds: float):
     """The oracle, as it stands, single-threaded, on a bounded sample: the
     first k rows of every matrix of the block, k grown until the timed pass
-    takes about `target_seconds`."""
+    takes about `target_seconds`.  The same sample is then run row-sharded
+    over every host core (`all_cores`)."""
     k = 1
     while True:
         sample = oracle_sample_step(wl, k)
@@ -709,10 +757,18 @@ def cpu_baseline(wl, target_seconds: float):
             break
         k = min(4096, max(k + 1, int(k * min(8.0, 1.2 * target_seconds / max(dt, 1e-3)))))
     weights = sum(s[0].size for s in sample)
+    cores = os.cpu_count() or 1
+    t = time.perf_counter()
+    oracle_step_sharded(wl, sample, 0, cores)
+    dt_all = time.perf_counter() - t
     return {"value": weights / dt, "unit": "weights/s", "cores": 1, "kind": "oracle",
             "sample": "first %d rows of each of the %d matrices (%d weights), one full "
                       "prior+forward+backward+compress pass, %.1f s" % (
-                          k, len(sample), weights, dt)}
+                          k, len(sample), weights, dt),
+            "cpu_model": cpu_model(),
+            "all_cores": {"value": weights / dt_all, "unit": "weights/s", "cores": cores,
+                          "sample": "the same sample, every matrix in %d row shards, one "
+                                    "thread per shard, %.2f s" % (cores, dt_all)}}
 
 
 def run_reference(args):
