@@ -718,8 +718,11 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
                                                  4 * q);
         };
         if (d.cpr > 0) {
+          // the same order as a lane-strided loop (lane, lane + 32, ...), with
+          // every load issued up front
           float v = 0.f;
-          for (int k = lane; k < Op::kConsumers; k += 32) v += part(k);
+#pragma unroll
+          for (int i = 0; i < Op::kConsumers / 32; ++i) v += part(lane + 32 * i);
           v = warp_sum(v);
           if (lane == 0) Op::write_row(d, c.row0, q, v);
         } else {
