@@ -407,6 +407,15 @@ maskllm_status maskllm_set_wait_timeout(uint64_t nanoseconds);
  * launches issued while enabled are invalid.  Host-global setting. */
 maskllm_status maskllm_test_withhold_loads(int32_t enable);
 
+/* Test hook for the sparse product (maskllm_spmm): a tile of C is 256 rows by
+ * a width the library picks per call from 256, 224, 192, 160, 128 columns
+ * against the number of tile waves.  n = 128..256, a multiple of 32, makes
+ * every later call use width n; n = 0 restores the choice per call.  Results
+ * are the same for every width (up to the fp32 summation order the tensor
+ * cores use).  MASKLLM_ERR_INVALID_ARG for any other n.  Host-global
+ * setting. */
+maskllm_status maskllm_test_spmm_tile_n(int32_t n);
+
 /* Waits for `stream`, then reads and clears the library's device error words
  * on the current device.  Returns MASKLLM_ERR_TIMEOUT if a bounded wait inside
  * a kernel gave up since the last call (its results are then invalid),

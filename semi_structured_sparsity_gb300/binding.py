@@ -30,7 +30,8 @@ EXPORTS = ("maskllm_prior_init", "maskllm_forward", "maskllm_backward",
            "maskllm_perm_swap_gains", "maskllm_perm_search", "maskllm_perm_search_static",
            "maskllm_spmm", "maskllm_forward_stats",
            "maskllm_set_wait_timeout",
-           "maskllm_test_withhold_loads", "maskllm_device_status", "maskllm_status_string",
+           "maskllm_test_withhold_loads", "maskllm_test_spmm_tile_n", "maskllm_device_status",
+           "maskllm_status_string",
            "maskllm_last_cuda_error", "maskllm_perm_workspace_bytes")
 MAX_BATCH = 16
 PERM_BAD_PERMUTATION = -1   # maskllm_perm_search / maskllm_perm_swap_gains outcome codes
@@ -86,6 +87,7 @@ def lib() -> C.CDLL:
         L.maskllm_mask_stats.argtypes = [vp, vp, i64, i64, f32, f32, maskllm_rng, vp, vp, vp, vp]
         L.maskllm_set_wait_timeout.argtypes = [u64]
         L.maskllm_test_withhold_loads.argtypes = [i32]
+        L.maskllm_test_spmm_tile_n.argtypes = [i32]
         L.maskllm_perm_shift.argtypes = [vp, i64, i64, vp, vp]
         L.maskllm_perm_metric.argtypes = [vp, i64, i64, vp, vp, vp, vp]
         L.maskllm_permute_columns.argtypes = [vp, i64, i64, vp, vp, vp]
@@ -293,6 +295,12 @@ def maskllm_set_wait_timeout(nanoseconds: int) -> None:
 
 def maskllm_test_withhold_loads(enable: bool) -> None:
     _check("maskllm_test_withhold_loads", lib().maskllm_test_withhold_loads(int(bool(enable))))
+
+
+def maskllm_test_spmm_tile_n(n: int) -> None:
+    """Force the sparse product's tile width (128..256, a multiple of 32), or
+    restore the per-call choice with 0 (test hook)."""
+    _check("maskllm_test_spmm_tile_n", lib().maskllm_test_spmm_tile_n(int(n)))
 
 
 def maskllm_prior_from_mask(meta, rows, cols, high, low, logits_out=None, stream=None):

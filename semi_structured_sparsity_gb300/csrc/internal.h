@@ -119,6 +119,9 @@ cudaError_t read_and_clear_perm_error(cudaStream_t s, uint32_t* value);
 // C [M, N] fp32 = A B^T, A as values bf16 [M, K/2] + codes u32 [M, K/32],
 // B bf16 [N, K].  Returns cudaErrorInvalidValue when the tensor maps cannot
 // be encoded.
+// Test hook: every later sparse product uses tile width n (128..256, a
+// multiple of 32), or chooses it per call again when n == 0.
+void spmm_force_tile_width(int n);
 cudaError_t spmm(const Device& d, const uint16_t* values, const uint32_t* meta, int64_t M,
                  int64_t K, const uint16_t* B, int64_t N, float* C, uint64_t wait_ns,
                  cudaStream_t s);

@@ -35,8 +35,12 @@
 //              built from the plain row-major codes with two byte permutes.
 //   warps 4-11 the epilogue: tensor memory -> registers -> shared memory
 //              (32-column boxes, 128-byte swizzle) -> bulk tensor stores of
-//              C, each box sent as soon as it is staged (columns 0..127 by
-//              warps 4-7, 128..255 by warps 8-11).
+//              C, each box sent as soon as it is staged (the first half of
+//              the tile's columns by warps 4-7, the rest by warps 8-11).
+// The tile is bn columns wide (bn = 256, 224, ..., 128, each CTA holding bn/2
+// rows of B): the host picks the width that minimises the modelled time of
+// the tile waves, e.g. 224 for 4096 x 4096 (304 tiles = 4 full waves of 76
+// pairs instead of 256 tiles = 3.4 waves; 94.5 against 96.6 us).
 // Every wait is bounded (pipeline.cuh); on a timeout the CTA raises its own
 // and its peer's abort flag and the device error word, waits (bounded) for
 // copies and MMAs in flight, and the pair frees its tensor memory together.
@@ -45,6 +49,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -61,13 +66,15 @@ namespace {
 // A CTA pair computes one 256 x 256 tile of C: CTA rank r of the cluster owns
 // rows 128 r .. 128 r + 127 of the tile (its own A rows, its own accumulator
 // lanes) and holds rows 128 r .. 128 r + 127 of the tile's 256 B rows.
+// kBN is the widest tile of C; a launch takes a width bn <= kBN (a multiple
+// of 32) chosen against the number of tile waves (spmm_tile_width)
 constexpr int kPairM = 256, kBM = 128, kBN = 256, kBNHalf = 128;
 constexpr int kBK = 128;      // dense K per stage: four K = 32 MMAs
 constexpr int kHalfK = 64;    // dense K per copy box (one 128-byte row of B)
 constexpr int kStages = 4;
 constexpr int kThreads = 384;
 constexpr uint32_t kABox = kBM * (kHalfK / 2) * 2;   // 8 KB: 128 rows x 32 values
-constexpr uint32_t kBBox = kBNHalf * kHalfK * 2;     // 16 KB: 128 rows x 64 values
+constexpr uint32_t kBBox = kBNHalf * kHalfK * 2;     // 16 KB: up to 128 rows x 64 values
 constexpr uint32_t kAStage = 2 * kABox, kBStage = 2 * kBBox;
 constexpr uint32_t kARowBytes = 64, kBRowBytes = 128;
 constexpr uint32_t kMetaBlock = 128 * 16;            // 16 bytes per tensor-memory lane
@@ -157,10 +164,9 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lead, uin
 constexpr uint32_t kSwizzleNone = 0, kSwizzle128 = 2, kSwizzle64 = 4;
 
 // Instruction descriptor: sparse (bit 2) with selector `sel`, fp32 D, bf16 A
-// and B, both K-major, N = 256, M = 256 (the pair's rows).
-__host__ __device__ constexpr uint32_t idesc_sparse(uint32_t sel) {
-  return (sel & 3u) | (1u << 2) | (1u << 4) | (1u << 7) | (1u << 10) |
-         ((static_cast<uint32_t>(kBN) >> 3) << 17) |
+// and B, both K-major, N = bn, M = 256 (the pair's rows).
+__host__ __device__ constexpr uint32_t idesc_sparse(uint32_t sel, uint32_t bn) {
+  return (sel & 3u) | (1u << 2) | (1u << 4) | (1u << 7) | (1u << 10) | ((bn >> 3) << 17) |
          ((static_cast<uint32_t>(kPairM) >> 4) << 24);
 }
 
@@ -211,8 +217,8 @@ __device__ __forceinline__ void raise(volatile int* abort_flag, uint32_t peer) {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     spmm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const __grid_constant__ CUtensorMap map_c, const uint32_t* __restrict__ meta,
-                float* __restrict__ C, int32_t M, int32_t N, int32_t K, int32_t tma_store,
-                uint64_t wait_ns) {
+                float* __restrict__ C, int32_t M, int32_t N, int32_t K, int32_t bn,
+                int32_t tma_store, uint64_t wait_ns) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base (the same offset in every CTA)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -230,7 +236,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
   const int m0 = (blockIdx.x >> 1) * kPairM + static_cast<int>(rank) * kBM;   // this CTA's rows
-  const int n0 = blockIdx.y * kBN;
+  const int n0 = blockIdx.y * bn;
+  const uint32_t b_box = static_cast<uint32_t>(bn / 2) * kHalfK * 2;   // this CTA's B rows
   const int nk = (K + kBK - 1) / kBK;
   const int kw = K / 32;   // K % 32 == 0: metadata words per row
 
@@ -240,12 +247,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int s = kt % kStages;
     const int nbox = (K - kt * kBK > kHalfK) ? 2 : 1;
     const uint32_t bar = smem_u32(&full[s]);
-    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nbox) * (kABox + kBBox));
+    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nbox) * (kABox + b_box));
     for (int h = 0; h < nbox; ++h) {
       tma_load_2d(sA + s * kAStage + h * kABox, &map_a, kt * (kBK / 2) + h * (kHalfK / 2), m0,
                   bar);
       tma_load_2d(sB + s * kBStage + h * kBBox, &map_b, kt * kBK + h * kHalfK,
-                  n0 + static_cast<int>(rank) * kBNHalf, bar);
+                  n0 + static_cast<int>(rank) * (bn / 2), bar);
     }
   };
   if (threadIdx.x == 0) {
@@ -331,7 +338,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               smem_desc(a + h * kABox + sub * 32, 0, 8 * kARowBytes, kSwizzle64);
           const uint64_t bd =
               smem_desc(b + h * kBBox + sub * 64, 0, 8 * kBRowBytes, kSwizzle128);
-          mma_sparse_pair(tmem, ad, bd, meta_t + 64u * h, idesc_sparse(sub), (kt | kb) != 0);
+          mma_sparse_pair(tmem, ad, bd, meta_t + 64u * h,
+                          idesc_sparse(sub, static_cast<uint32_t>(bn)), (kt | kb) != 0);
         }
         mma_commit_pair_both(&empty[s]);
       }
@@ -339,8 +347,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mma_commit_pair_both(done);
     }
   } else if (warp >= 4) {
-    // ---- warps 4-7: metadata, then the epilogue of columns 0..127;
-    //      warps 8-11: the epilogue of columns 128..255.  Thread q of a
+    // ---- warps 4-7: metadata, then the epilogue of the tile's first
+    //      columns; warps 8-11: the epilogue of the others.  Thread q of a
     //      group owns tensor-memory lane q. ----
     const int g = (warp - 4) >> 2;
     const int q = (threadIdx.x - 128) & 127;
@@ -399,9 +407,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (ok) tc_fence_after();
     const int m = m0 + q;
     float* crow = C + static_cast<int64_t>(m) * N;
+    // bn / 32 boxes of 32 columns: the first half (rounded up) for group 0
+    const int nb = bn / 32, nb0 = (nb + 1) / 2;
+    const int cb_end = g == 0 ? nb0 : nb - nb0;
 #pragma unroll 1
-    for (int cb = 0; cb < kBN / 64; ++cb) {
-      const int c = (kBN / 64) * g + cb;   // box of columns 32 c .. 32 c + 31
+    for (int cb = 0; cb < cb_end; ++cb) {
+      const int c = g * nb0 + cb;   // box of columns 32 c .. 32 c + 31
       if (ok) {
         uint32_t v[32];
         asm volatile(
@@ -501,15 +512,45 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType type, uint32_t elem_bytes, c
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tile width of C for an M x N x K product on `sms` SMs: the width w in 256,
+// 224, 192, 160, 128 with the least modelled time, waves(w) * (7.2 + K /
+// 4096 * (12.6 + 0.0172 w)) microseconds per wave of CTA pairs -- fitted to
+// the measured times of every width on 4096 x 4096 x 4096 and 4096 x 11008 x
+// 4096 (a narrower tile saves little per wave: the per-stage waits, commits
+// and copies of A do not shrink with it) -- the wider tile on a tie.
+int spmm_tile_width(int64_t M, int64_t N, int64_t K, int sms) {
+  const int64_t pairs = std::max<int64_t>(1, sms / 2);
+  const int64_t rows = (M + kPairM - 1) / kPairM;
+  int best = kBN;
+  double best_t = 0.0;
+  for (int w = kBN; w >= 128; w -= 32) {
+    const int64_t tiles = rows * ((N + w - 1) / w);
+    const int64_t waves = (tiles + pairs - 1) / pairs;
+    const double t = static_cast<double>(waves) *
+                     (7.2 + static_cast<double>(K) / 4096.0 * (12.6 + 0.0172 * w));
+    if (w == kBN || t < best_t) {
+      best = w;
+      best_t = t;
+    }
+  }
+  return best;
+}
+
+int g_spmm_tile_n = 0;   // test hook: a forced tile width, 0 = chosen per call
+
 }  // namespace
 
-cudaError_t spmm(const Device&, const uint16_t* values, const uint32_t* meta, int64_t M, int64_t K,
-                 const uint16_t* B, int64_t N, float* C, uint64_t wait_ns, cudaStream_t s) {
+void spmm_force_tile_width(int n) { g_spmm_tile_n = n; }
+
+cudaError_t spmm(const Device& d, const uint16_t* values, const uint32_t* meta, int64_t M,
+                 int64_t K, const uint16_t* B, int64_t N, float* C, uint64_t wait_ns,
+                 cudaStream_t s) {
+  const int bn = g_spmm_tile_n != 0 ? g_spmm_tile_n : spmm_tile_width(M, N, K, d.num_sms);
   CUtensorMap map_a, map_b, map_c;
   if (!make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, values, M, K / 2, kHalfK / 2, kBM,
                 CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, kHalfK, kBNHalf,
-                CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, kHalfK,
+                static_cast<uint32_t>(bn / 2), CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // C leaves through bulk stores when its rows are 16-byte multiples on a
   // 16-byte aligned base; otherwise each thread stores its row directly
@@ -522,11 +563,11 @@ cudaError_t spmm(const Device&, const uint16_t* values, const uint32_t* meta, in
   cudaError_t e =
       cudaFuncSetAttribute(spmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  // x: two CTAs (one cluster) per 256 rows of C; y: 256 columns of C
+  // x: two CTAs (one cluster) per 256 rows of C; y: bn columns of C
   const dim3 grid(static_cast<unsigned>(2 * ((M + kPairM - 1) / kPairM)),
-                  static_cast<unsigned>((N + kBN - 1) / kBN));
+                  static_cast<unsigned>((N + bn - 1) / bn));
   spmm_kernel<<<grid, kThreads, smem, s>>>(map_a, map_b, map_c, meta, C, static_cast<int32_t>(M),
-                                           static_cast<int32_t>(N), static_cast<int32_t>(K),
+                                           static_cast<int32_t>(N), static_cast<int32_t>(K), bn,
                                            tma_store ? 1 : 0, wait_ns);
   return cudaGetLastError();
 }

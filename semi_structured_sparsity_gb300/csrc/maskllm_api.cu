@@ -690,6 +690,12 @@ maskllm_status maskllm_test_withhold_loads(int32_t enable) {
   return MASKLLM_OK;
 }
 
+maskllm_status maskllm_test_spmm_tile_n(int32_t n) {
+  if (n != 0 && (n < 128 || n > 256 || n % 32 != 0)) return MASKLLM_ERR_INVALID_ARG;
+  maskllm::spmm_force_tile_width(n);
+  return MASKLLM_OK;
+}
+
 maskllm_status maskllm_device_status(maskllm_stream_t stream) {
   uint32_t a = 0, b = 0, c = 0;
   cudaError_t e = maskllm::read_and_clear_error_word(stream, &a);

@@ -206,6 +206,13 @@ def test_spmm_validation(L):
     assert L.maskllm_spmm(A, B, 128, 64, Cc, 256, Cc + 64, None) == ALIAS  # C over B
 
 
+def test_spmm_tile_hook_validation(L):
+    for n in (100, 129, 288, -32, 96):
+        assert L.maskllm_test_spmm_tile_n(n) == INVALID
+    for n in (128, 160, 192, 224, 256, 0):
+        assert L.maskllm_test_spmm_tile_n(n) == 0
+
+
 def test_forward_stats_validation(L):
     r = _rng()
     f = L.maskllm_forward_stats

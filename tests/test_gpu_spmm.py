@@ -92,6 +92,24 @@ def test_output_not_16_byte_aligned_is_rejected():
     assert mk.maskllm_device_status() == 0
 
 
+@pytest.mark.parametrize("width", [128, 160, 192, 224, 256])
+def test_every_tile_width_bit_exact(width):
+    """The tile width (columns of C per CTA pair) is chosen per call; each
+    width, forced, gives the exact product on ragged shapes: 700 columns
+    leave a partial last tile for every width, 300 rows a partial pair."""
+    M, K, N = 300, 192, 700
+    vals, meta, Bb = operands(M, K, N, width, integers=True)
+    try:
+        mk.maskllm_test_spmm_tile_n(width)
+        C = mk.maskllm_spmm(*to_gpu(vals, meta, Bb))
+        torch.cuda.synchronize()
+    finally:
+        mk.maskllm_test_spmm_tile_n(0)
+    want, _ = orc.spmm(vals, meta, M, K, Bb)
+    assert np.array_equal(C.cpu().numpy().astype(np.float64), want)
+    assert mk.maskllm_device_status() == 0
+
+
 def test_two_calls_in_a_row_and_output_overwritten():
     vals, meta, Bb = operands(256, 256, 512, 3, integers=True)
     v, m, b = to_gpu(vals, meta, Bb)
