@@ -293,7 +293,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         issued = kt + 1;
       }
       if (*abort_flag) {
-        // wait (bounded) for the copies still landing in this CTA
+        // wait (bounded) for the copies still landing in this CTA.  Rank 0's
+        // stage barrier also counts arrivals from the metadata warps and
+        // rank 1 that an abort may have stopped: such a wait runs to its
+        // limit (up to kStages x wait_ns in all), long after the copies
+        // themselves have landed.
         for (int kt = issued > kStages ? issued - kStages : 0; kt < issued; ++kt) {
           int never = 0;
           mbar_wait_bounded(&full[kt % kStages], (kt / kStages) & 1, wait_ns, &never);
