@@ -502,17 +502,23 @@ __global__ void __launch_bounds__(256) perm_rows_kernel(const uint32_t* __restri
     __syncthreads();
     if (c < cols) {
       int rr = 0;
-      for (; rr + 1 < n; rr += 2) {
-        const uint2 v = *reinterpret_cast<const uint2*>(V + (rc + rr) * cols + c);
-        const uint2 w = *reinterpret_cast<const uint2*>(V + (rc + rr + 1) * cols + c);
+      // eight rows' loads in flight per thread before any is used
+      for (; rr + 7 < n; rr += 8) {
+        uint2 v[8];
 #pragma unroll
-        for (int i = 0; i < 6; ++i) {
-          const uint32_t s = sx[rr][i], u = sx[rr + 1][i];
-          acc[i][0] += max(s, v.x) + max(u, w.x);
-          acc[i][1] += max(s, v.y) + max(u, w.y);
+        for (int j = 0; j < 8; ++j)
+          v[j] = *reinterpret_cast<const uint2*>(V + (rc + rr + j) * cols + c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+          for (int i = 0; i < 6; ++i) {
+            const uint32_t s = sx[rr + j][i];
+            acc[i][0] += max(s, v[j].x);
+            acc[i][1] += max(s, v[j].y);
+          }
         }
       }
-      if (rr < n) {
+      for (; rr < n; ++rr) {
         const uint2 v = *reinterpret_cast<const uint2*>(V + (rc + rr) * cols + c);
 #pragma unroll
         for (int i = 0; i < 6; ++i) {
