@@ -693,7 +693,10 @@ cudaError_t perm_search(const Device& d, const uint16_t* W, int64_t rows, int64_
   const dim3 best_grid(static_cast<unsigned>(nt), static_cast<unsigned>(nt));
   const int apply_blocks = blocks_for(rows > cols ? rows : cols, 256, 1LL << 30);
   const int col_blocks = static_cast<int>((cols + 511) / 512);
-  int64_t slices = (2LL * d.num_sms + col_blocks - 1) / col_blocks;
+  // about four blocks of row slices per SM (eight rows' loads in flight per
+  // thread); twice as many slices measured slower: their partial rows cost
+  // more integer atomics than the extra blocks hide
+  int64_t slices = (4LL * d.num_sms + col_blocks - 1) / col_blocks;
   const int64_t max_slices = (rows + 31) / 32;
   if (slices > max_slices) slices = max_slices;
   if (slices < 1) slices = 1;
