@@ -350,20 +350,29 @@ __global__ void __launch_bounds__(256) perm_best_kernel(const uint32_t* __restri
   if (threadIdx.x < 32) dA[tx] = E[(a0 + tx) * (cols + 1)];
   else if (threadIdx.x < 64) dB[tx] = E[(b0 + tx) * (cols + 1)];
   __syncthreads();
-  unsigned long long best = 0;
+  // this thread's pairs come in increasing (a, b) order, so keeping the
+  // first strictly larger gain keeps the smallest index among equal gains;
+  // the 64-bit key is formed once, from the thread's best
+  const int ia0 = tA * 32, ib = tB * 32 + tx;   // slot numbers < 2^15
+  const int64_t db = dB[tx];
+  int64_t best_g = 0;
+  int best_i = 0;
+#pragma unroll
   for (int i = ty; i < 32; i += 8) {
-    const int64_t a = a0 + i, b = b0 + tx;
-    if (a < b && (a >> 2) != (b >> 2)) {
+    const int ia = ia0 + i;
+    if (ia < ib && (ia >> 2) != (ib >> 2)) {
       const int64_t g =
-          (static_cast<int64_t>(T[i][tx]) - dA[i]) + (static_cast<int64_t>(U[tx][i]) - dB[tx]);
-      if (g > 0) {
-        const unsigned long long key =
-            (static_cast<unsigned long long>(g) << kKeyIndexBits) |
-            (kKeyIndexMask - static_cast<unsigned long long>((a << 15) | b));
-        best = key > best ? key : best;
+          (static_cast<int64_t>(T[i][tx]) - dA[i]) + (static_cast<int64_t>(U[tx][i]) - db);
+      if (g > best_g) {
+        best_g = g;
+        best_i = (ia << 15) | ib;
       }
     }
   }
+  unsigned long long best =
+      best_g > 0 ? (static_cast<unsigned long long>(best_g) << kKeyIndexBits) |
+                       (kKeyIndexMask - static_cast<unsigned long long>(best_i))
+                 : 0ull;
   best = warp_max_u64(best);
   if (tx == 0) red[ty] = best;
   __syncthreads();
