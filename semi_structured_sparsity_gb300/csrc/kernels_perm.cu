@@ -325,83 +325,134 @@ __global__ void __launch_bounds__(256) perm_gains_kernel(const uint32_t* __restr
 // ---------------------------------------------------------------------------
 
 // The best swap: largest positive gain, then smallest a * 2^15 + b, as one
-// 64-bit key (gain << 30 | (2^30 - 1 - (a << 15 | b))).  One block per 32 x 32
-// tile of slot pairs with tA <= tB (the others return at once), so every
-// block's loads are in flight together; each block writes its largest key
-// (0: none) to its slot of `tile_best` (upper-triangle order), and the last
-// block to finish (a counter, no waiting) reduces them into ctl->key and
-// resets the counter.
+// 64-bit key (gain << 30 | (2^30 - 1 - (a << 15 | b))).  A persistent grid
+// walks the 32 x 32 tiles of slot pairs with tA <= tB (grid-stride over all
+// tA, tB; the others are skipped), double-buffering each tile pair's two E
+// tiles and diagonal entries with per-thread asynchronous copies so the next
+// tile's loads overlap this tile's gains.  Each thread keeps its best gain
+// and index, each block writes its largest key (0: none) to its slot of
+// `tile_best`, and the last block to finish (a counter, no waiting) reduces
+// them into ctl->key and resets the counter.
+struct BestTile {
+  uint32_t T[32][32];   // E[a0 + i][b0 + j], read along rows
+  uint32_t U[32][33];   // E[b0 + i][a0 + j], read along columns (padded)
+  uint32_t dA[32], dB[32];
+};
+
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __global__ void __launch_bounds__(256) perm_best_kernel(const uint32_t* __restrict__ E,
                                                         int32_t cols,
                                                         unsigned long long* __restrict__ tile_best,
                                                         PermCtl* ctl) {
   if (ctl->done) return;
-  const int tA = blockIdx.y, tB = blockIdx.x, nt = gridDim.x;
-  if (tA > tB) return;
-  __shared__ uint32_t T[32][33], U[32][33], dA[32], dB[32];
+  __shared__ __align__(16) BestTile buf[2];
   __shared__ unsigned long long red[8];
   __shared__ int last;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int64_t a0 = static_cast<int64_t>(tA) * 32, b0 = static_cast<int64_t>(tB) * 32;
-  for (int i = ty; i < 32; i += 8) {
-    T[i][tx] = E[(a0 + i) * cols + b0 + tx];
-    U[i][tx] = E[(b0 + i) * cols + a0 + tx];
-  }
-  if (threadIdx.x < 32) dA[tx] = E[(a0 + tx) * (cols + 1)];
-  else if (threadIdx.x < 64) dB[tx] = E[(b0 + tx) * (cols + 1)];
-  __syncthreads();
-  // this thread's pairs come in increasing (a, b) order, so keeping the
-  // first strictly larger gain keeps the smallest index among equal gains;
-  // the 64-bit key is formed once, from the thread's best
-  const int ia0 = tA * 32, ib = tB * 32 + tx;   // slot numbers < 2^15
-  const int64_t db = dB[tx];
+  const int nt = cols / 32;
+  const int ntiles = nt * nt;
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5, lane = tid & 31;
+  // the next tile pair with tA <= tB at or after t (grid stride), or ntiles
+  auto next_tile = [&](int t) {
+    while (t < ntiles && t / nt > t % nt) t += gridDim.x;
+    return t < ntiles ? t : ntiles;
+  };
+  auto issue = [&](int t, BestTile& b) {
+    const int64_t a0 = static_cast<int64_t>(t / nt) * 32, b0 = static_cast<int64_t>(t % nt) * 32;
+    // T: 32 rows x 128 bytes, one 16-byte piece per thread
+    const int r = tid >> 3, q = (tid & 7) * 4;
+    cp_async_16(&b.T[r][q], E + (a0 + r) * cols + b0 + q);
+    // U: 1024 words into the padded rows, four per thread
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = tid + 256 * k, rr = e >> 5, cc = e & 31;
+      cp_async_4(&b.U[rr][cc], E + (b0 + rr) * cols + a0 + cc);
+    }
+    if (tid < 32)
+      cp_async_4(&b.dA[tid], E + (a0 + tid) * (cols + 1));
+    else if (tid < 64)
+      cp_async_4(&b.dB[tid - 32], E + (b0 + tid - 32) * (cols + 1));
+  };
+
   int64_t best_g = 0;
   int best_i = 0;
+  int t = next_tile(blockIdx.x);
+  if (t < ntiles) issue(t, buf[0]);
+  cp_async_commit();
+  for (int k = 0; t < ntiles; ++k) {
+    const int tn = next_tile(t + gridDim.x);
+    if (tn < ntiles) issue(tn, buf[(k + 1) & 1]);
+    cp_async_commit();
+    cp_async_wait<1>();   // this tile's copies (all but the newest group)
+    __syncthreads();
+    const BestTile& b = buf[k & 1];
+    const int ia0 = (t / nt) * 32, ib = (t % nt) * 32 + tx;   // slot numbers < 2^15
+    const int64_t db = b.dB[tx];
 #pragma unroll
-  for (int i = ty; i < 32; i += 8) {
-    const int ia = ia0 + i;
-    if (ia < ib && (ia >> 2) != (ib >> 2)) {
-      const int64_t g =
-          (static_cast<int64_t>(T[i][tx]) - dA[i]) + (static_cast<int64_t>(U[tx][i]) - db);
-      if (g > best_g) {
-        best_g = g;
-        best_i = (ia << 15) | ib;
+    for (int i = ty; i < 32; i += 8) {
+      const int ia = ia0 + i;
+      if (ia < ib && (ia >> 2) != (ib >> 2)) {
+        const int64_t g =
+            (static_cast<int64_t>(b.T[i][tx]) - b.dA[i]) + (static_cast<int64_t>(b.U[tx][i]) - db);
+        const int idx = (ia << 15) | ib;
+        if (g > best_g || (g == best_g && g > 0 && idx < best_i)) {
+          best_g = g;
+          best_i = idx;
+        }
       }
     }
+    __syncthreads();   // before the next issue overwrites this buffer
+    t = tn;
   }
+  cp_async_wait<0>();
   unsigned long long best =
       best_g > 0 ? (static_cast<unsigned long long>(best_g) << kKeyIndexBits) |
                        (kKeyIndexMask - static_cast<unsigned long long>(best_i))
                  : 0ull;
   best = warp_max_u64(best);
-  if (tx == 0) red[ty] = best;
+  if (lane == 0) red[ty] = best;
   __syncthreads();
-  const uint32_t n_up = static_cast<uint32_t>(nt) * (nt + 1) / 2;
-  if (threadIdx.x == 0) {
+  const uint32_t nblocks = gridDim.x;
+  if (tid == 0) {
     unsigned long long m = 0;
     for (int w = 0; w < 8; ++w) m = red[w] > m ? red[w] : m;
-    // upper-triangle index of (tA, tB)
-    const int64_t idx = static_cast<int64_t>(tA) * nt - static_cast<int64_t>(tA) * (tA - 1) / 2 +
-                        (tB - tA);
-    tile_best[idx] = m;
+    tile_best[blockIdx.x] = m;
     __threadfence();
-    last = atomicAdd(&ctl->tiles_done, 1u) == n_up - 1;
+    last = atomicAdd(&ctl->tiles_done, 1u) == nblocks - 1;
   }
   __syncthreads();
   if (!last) return;
   __threadfence();
   unsigned long long m = 0;
-  for (uint32_t i = threadIdx.x; i < n_up; i += blockDim.x) {
-    const unsigned long long k = *reinterpret_cast<volatile const unsigned long long*>(tile_best + i);
-    m = k > m ? k : m;
+  for (uint32_t i = tid; i < nblocks; i += blockDim.x) {
+    const unsigned long long kk = *reinterpret_cast<volatile const unsigned long long*>(tile_best + i);
+    m = kk > m ? kk : m;
   }
   m = warp_max_u64(m);
-  if (tx == 0) red[ty] = m;
+  if (lane == 0) red[ty] = m;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    unsigned long long k = 0;
-    for (int w = 0; w < 8; ++w) k = red[w] > k ? red[w] : k;
-    ctl->key = k;
+  if (tid == 0) {
+    unsigned long long kk = 0;
+    for (int w = 0; w < 8; ++w) kk = red[w] > kk ? red[w] : kk;
+    ctl->key = kk;
     ctl->tiles_done = 0;
   }
 }
@@ -698,8 +749,12 @@ cudaError_t perm_search(const Device& d, const uint16_t* W, int64_t rows, int64_
   cudaError_t e = prepare_table(d, W, rows, cols, perm, w, s);
   if (e != cudaSuccess) return e;
   const int32_t c = static_cast<int32_t>(cols);
+  // persistent scan: four blocks per SM, at most one per tile pair and no
+  // more than tile_best holds (nt (nt + 1) / 2 slots)
   const int64_t nt = cols / 32;
-  const dim3 best_grid(static_cast<unsigned>(nt), static_cast<unsigned>(nt));
+  int64_t best_blocks = 4LL * d.num_sms;
+  if (best_blocks > nt * (nt + 1) / 2) best_blocks = nt * (nt + 1) / 2;
+  const unsigned best_grid = static_cast<unsigned>(best_blocks);
   const int apply_blocks = blocks_for(rows > cols ? rows : cols, 256, 1LL << 30);
   const int col_blocks = static_cast<int>((cols + 511) / 512);
   // about four blocks of row slices per SM (eight rows' loads in flight per
