@@ -31,9 +31,10 @@
 // the rows, computed by a tiled kernel; after a swap of slots a and b the
 // columns a and b of V, hence of E, trade places, and S changes only for the
 // three group-mates of a and of b, whose six rows of E are recomputed.  One
-// search step is three kernels: best (the largest gain of every 32 x 32 tile
-// of pairs, then of those), apply (the swap and the cheap updates), rows (the
-// six E rows).  All of them return at once when the search has stopped,
+// search step is three kernels: best (a persistent scan of the 32 x 32 tiles
+// of pairs, each block's largest gain, then the largest of those), apply (the
+// swap and the cheap updates), rows (the six E rows).  All of them return at
+// once when the search has stopped,
 // so the host enqueues max_swaps steps without waiting for any of them.
 #include <cuda_runtime.h>
 #include <stdint.h>
