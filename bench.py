@@ -51,6 +51,9 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--spmm-tile-n", type=int, default=0,
+                    help="force the sparse product's tile width (128..256, a multiple of 32) "
+                         "for the spmm extra; 0 = the width the library picks per call")
     ap.add_argument("--only", default=None,
                     help="comma-separated matrix names of the workload to run (e.g. 'down'); "
                          "for small profiling runs")
@@ -356,7 +359,7 @@ def run_gpu(args):
     if (dominant, shape_key) in tt and tt[(dominant, shape_key)][1] == digest:
         traffic = tt[(dominant, shape_key)][0]
 
-    extras = run_extras(blk, peak, dev)
+    extras = run_extras(blk, peak, dev, spmm_tile_n=args.spmm_tile_n)
 
     e2e = None
     if not args.no_e2e:
@@ -405,7 +408,7 @@ def run_gpu(args):
     ranks.close()
 
 
-def run_extras(blk, peak, dev, reps=20):
+def run_extras(blk, peak, dev, reps=20, spmm_tile_n=0):
     """The entry points beyond the step, on the same resident block: logits
     from a given mask (6.125 B/weight: codes in, logits out), the convergence
     diagnostics (6.5 B/weight: logits and previous draws in, draws out) and
@@ -467,7 +470,12 @@ def run_extras(blk, peak, dev, reps=20):
                      "frac_of_hbm": round(gbs / peak, 4), "bytes_per_weight": bpw,
                      "launches_per_block": len(blk.mats)}
     out["perm_search"] = run_perm_search(blk, dev)
-    out["spmm"] = run_spmm(blk, dev)
+    blk.mk.maskllm_test_spmm_tile_n(spmm_tile_n)
+    try:
+        out["spmm"] = run_spmm(blk, dev)
+    finally:
+        blk.mk.maskllm_test_spmm_tile_n(0)
+    out["spmm"]["tile_n"] = spmm_tile_n if spmm_tile_n else "chosen per call"
     return out
 
 
