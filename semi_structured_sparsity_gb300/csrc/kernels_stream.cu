@@ -670,16 +670,22 @@ struct FwdStatsOp : OpBase<GPT, 4> {
       // diagnostics
       const int s = first_argmax6(z);
       drawn |= static_cast<uint32_t>(s) << (8 * k);
-      if (d.G != nullptr) {
-        const uint32_t q = (prev >> (8 * k)) & 7u;   // entries 6, 7 count as empty masks
-        acc[1] += static_cast<float>(
-            __popc(((kKeepBits >> (4 * s)) ^ (kKeepBits >> (4 * q))) & 0xFu));
-      }
       const float my = fmaxf(fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3])), fmaxf(y[4], y[5]));
       float sum = 0.f;
 #pragma unroll
       for (int c6 = 0; c6 < kCand; ++c6) sum += ex2_approx((y[c6] - my) * kLog2e);
       acc[2] += rcp_approx(sum);   // the largest term is 2^0 = 1
+    }
+    // the previous draws are used last, so their load has the most work to
+    // hide behind (integer counts: the order of the additions is immaterial)
+    if (d.G != nullptr) {
+#pragma unroll
+      for (int k = 0; k < GPT; ++k) {
+        const uint32_t s = (drawn >> (8 * k)) & 0xFFu;
+        const uint32_t q = (prev >> (8 * k)) & 7u;   // entries 6, 7 count as empty masks
+        acc[1] += static_cast<float>(
+            __popc(((kKeepBits >> (4 * s)) ^ (kKeepBits >> (4 * q))) & 0xFu));
+      }
     }
     store_w_global<GPT>(d.out0, unit, o);
     if (d.out2 != nullptr) static_cast<uint16_t*>(d.out2)[unit] = static_cast<uint16_t>(drawn);
