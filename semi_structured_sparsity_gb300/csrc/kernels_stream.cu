@@ -277,6 +277,10 @@ struct OpBase {
   // store queued behind the refill's copies leaves the stage later (the
   // prior measured 17% slower that way).
   static constexpr bool kRefillFirst = false;
+  // long rows: each consumer warp leaves one partial (the sum of its lanes')
+  // in its lane 0's slot and the producer adds kConsumerWarps values; else
+  // every thread leaves its own partial and the producer adds kConsumers
+  static constexpr bool kWarpRowSums = false;
 };
 
 template <int GPT>
@@ -320,6 +324,8 @@ struct FwdOp : OpBase<GPT, 4> {
   static constexpr bool kTable = true, kStaged = false, kWarpWide = false;
   static constexpr bool kOutOverlapsInput = false;
   static constexpr bool kRefillFirst = true;
+  // forward 393.8 -> 380.8 us; the diagnostics measured slower with it
+  static constexpr bool kWarpRowSums = true;
   // row sum of squares; each thread's partial in a region of its own after
   // the logits, so the refill can land while the producer reduces them
   static constexpr int kRowQuantities = 1;
@@ -730,9 +736,16 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
           return *reinterpret_cast<const float*>(st + Op::kPartOffset + k * Op::kPartStride +
                                                  4 * q);
         };
-        if (d.cpr > 0) {
-          // the same order as a lane-strided loop (lane, lane + 32, ...), with
-          // every load issued up front
+        if (d.cpr > 0 && Op::kWarpRowSums) {
+          // one partial per consumer warp (each already its warp's sum, in
+          // the slot of the warp's lane 0)
+          static_assert(Op::kConsumerWarps <= 32, "one warp sum per lane");
+          float v = lane < Op::kConsumerWarps ? part(32 * lane) : 0.f;
+          v = warp_sum(v);
+          if (lane == 0) Op::write_row(d, c.row0, q, v);
+        } else if (d.cpr > 0) {
+          // the same order as a lane-strided loop (lane, lane + 32, ...),
+          // with every load issued up front
           float v = 0.f;
 #pragma unroll
           for (int i = 0; i < Op::kConsumers / 32; ++i) v += part(lane + 32 * i);
@@ -864,10 +877,24 @@ __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
     else if (Op::kGPT * t < c.ng)
       Op::consume(p, d, c, st, t, tab, acc);
     if (Op::kRowQuantities > 0) {
-      float* part = reinterpret_cast<float*>(st + Op::kPartOffset + t * Op::kPartStride);
-      if (d.cpr == 0 || c.nrows > 0) {
-        // the row ends in this chunk (long rows), or each thread's groups lie
-        // in one short row of this chunk
+      if (Op::kWarpRowSums && d.cpr > 0) {
+        if (c.nrows > 0) {
+          // the row ends in this chunk: each warp leaves the sum of its
+          // lanes' partials in its lane 0's slot (a slot that thread has
+          // consumed itself), so the producer adds only kConsumerWarps values
+          float* part =
+              reinterpret_cast<float*>(st + Op::kPartOffset + (t & ~31) * Op::kPartStride);
+#pragma unroll
+          for (int q = 0; q < Op::kRowQuantities; ++q) {
+            const float v = warp_sum(acc[q]);
+            if (lane == 0) part[q] = v;
+            acc[q] = 0.f;
+          }
+        }
+      } else if (d.cpr == 0 || c.nrows > 0) {
+        // the row ends in this chunk (long rows), or each thread's groups
+        // lie in one short row of this chunk: each thread's own partial
+        float* part = reinterpret_cast<float*>(st + Op::kPartOffset + t * Op::kPartStride);
 #pragma unroll
         for (int q = 0; q < Op::kRowQuantities; ++q) {
           part[q] = acc[q];
