@@ -50,6 +50,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -540,16 +541,19 @@ int spmm_tile_width(int64_t M, int64_t N, int64_t K, int sms) {
   return best;
 }
 
-int g_spmm_tile_n = 0;   // test hook: a forced tile width, 0 = chosen per call
+// test hook: a forced tile width, 0 = chosen per call (set and read from any
+// host thread)
+std::atomic<int> g_spmm_tile_n{0};
 
 }  // namespace
 
-void spmm_force_tile_width(int n) { g_spmm_tile_n = n; }
+void spmm_force_tile_width(int n) { g_spmm_tile_n.store(n, std::memory_order_relaxed); }
 
 cudaError_t spmm(const Device& d, const uint16_t* values, const uint32_t* meta, int64_t M,
                  int64_t K, const uint16_t* B, int64_t N, float* C, uint64_t wait_ns,
                  cudaStream_t s) {
-  const int bn = g_spmm_tile_n != 0 ? g_spmm_tile_n : spmm_tile_width(M, N, K, d.num_sms);
+  const int forced = g_spmm_tile_n.load(std::memory_order_relaxed);
+  const int bn = forced != 0 ? forced : spmm_tile_width(M, N, K, d.num_sms);
   CUtensorMap map_a, map_b, map_c;
   if (!make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, values, M, K / 2, kHalfK / 2, kBM,
                 CU_TENSOR_MAP_SWIZZLE_64B) ||
