@@ -57,13 +57,7 @@ def parse_args(argv=None):
     ap.add_argument("--only", default=None,
                     help="comma-separated matrix names of the workload to run (e.g. 'down'); "
                          "for small profiling runs")
-    ap.add_argument("--kernels", choices=("stream", "direct"), default="stream",
-                    help="stream: pipelined batched kernels; direct: per-matrix kernels with "
-                         "direct vector loads (same results, for comparison)")
-    args = ap.parse_args(argv)
-    if args.kernels == "direct":
-        os.environ["MASKLLM_KERNELS"] = "direct"
-    return args
+    return ap.parse_args(argv)
 
 
 # ---------------------------------------------------------------------------
@@ -263,9 +257,7 @@ class Block:
         self.arr = mk.matrix_array(self.mats)
         self.n = len(self.mats)
         self.weights = sum(m["x"].rows * m["x"].cols for m in self.mats)
-        direct = os.environ.get("MASKLLM_KERNELS") == "direct"
-        per_call = self.n if direct else (self.n + mk.MAX_BATCH - 1) // mk.MAX_BATCH
-        self.launches_per_call = per_call
+        self.launches_per_call = (self.n + mk.MAX_BATCH - 1) // mk.MAX_BATCH
         self.launches = 0
 
     def outputs(self, m):
@@ -396,7 +388,6 @@ def run_gpu(args):
                      "bytes_per_launch": BYTES_PER_WEIGHT[dominant] * blk.weights
                      / blk.launches_per_call,
                      "launches_per_step": blk.launches_per_call},
-        "kernel_variant": args.kernels,
         "extras": extras,
         "gpu_launches": launches,
         "clocks": clk,
@@ -620,17 +611,28 @@ def run_e2e(args, blk, ranks, dev, only=None):
     d2h = sum(t.numel() * t.element_size() for h in host_out for t in h)
     s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
+    # per step: (start, end) events around its H2D copies and its D2H copies,
+    # recorded after the waits, so each pair spans the copies alone
+    copy_ev = {"h2d": [], "d2h": []}
 
-    def one(step):
+    def timing_pair():
+        return (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+
+    def one(step, timed=False):
         x_i = step % 2
         b = sets[x_i]
         with torch.cuda.stream(s_in):
             if step >= 2:
                 s_in.wait_event(ev["comp"][x_i])      # step - 2 has read these inputs
+            if timed:
+                copy_ev["h2d"].append(timing_pair())
+                copy_ev["h2d"][-1][0].record(s_in)
             for m, hin in zip(b.mats, host_in):
                 x = m["x"]
                 for dst, src in zip((x.W, x.L, x.G), hin):
                     dst.copy_(src, non_blocking=True)
+            if timed:
+                copy_ev["h2d"][-1][1].record(s_in)
             ev["in"][x_i].record(s_in)
         with torch.cuda.stream(s_comp):
             s_comp.wait_event(ev["in"][x_i])
@@ -640,9 +642,14 @@ def run_e2e(args, blk, ranks, dev, only=None):
             ev["comp"][x_i].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev["comp"][x_i])
+            if timed:
+                copy_ev["d2h"].append(timing_pair())
+                copy_ev["d2h"][-1][0].record(s_out)
             for m, hout in zip(b.mats, host_out):
                 for dst, src in zip(hout, b.outputs(m)):
                     dst.copy_(src, non_blocking=True)
+            if timed:
+                copy_ev["d2h"][-1][1].record(s_out)
             ev["out"][x_i].record(s_out)
 
     for w in range(2):
@@ -655,15 +662,23 @@ def run_e2e(args, blk, ranks, dev, only=None):
     s_comp.wait_event(t0)
     s_out.wait_event(t0)
     for st in range(args.e2e_steps):
-        one(st + 2)
+        one(st + 2, timed=True)
     t1.record(s_out)
     torch.cuda.synchronize(dev)
     ranks.barrier()
     sec = ranks.max(t0.elapsed_time(t1) / 1e3)
+    # achieved host-link rates of the timed steps: bytes over the summed
+    # durations of each step's copies (the copies of one direction are
+    # serialised on their stream, so the sum is that direction's busy time)
+    h2d_s = sum(a.elapsed_time(b) for a, b in copy_ev["h2d"]) / 1e3
+    d2h_s = sum(a.elapsed_time(b) for a, b in copy_ev["d2h"]) / 1e3
     del sets[1]
     return {"value": job_value(blk.weights, ranks.world, sec, args.e2e_steps),
             "unit": "weights/s", "steps": args.e2e_steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_gbs": round(h2d * args.e2e_steps / h2d_s / 1e9, 1),
+            "d2h_gbs": round(d2h * args.e2e_steps / d2h_s / 1e9, 1),
+            "ms_per_step": round(sec / args.e2e_steps * 1e3, 3),
             "pipelining": "2 device buffer sets; H2D, kernels and D2H of consecutive steps on "
                           "3 streams"}
 

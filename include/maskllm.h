@@ -321,9 +321,12 @@ maskllm_status maskllm_spmm(const uint16_t* values, const uint32_t* meta, int64_
  * (for example cols = 1024 with rows above 3583, or cols = 2048 with rows
  * above 1022) returns MASKLLM_ERR_SHAPE and launches nothing.
  *
- * The first call on a device looks up the array's device address (once per
- * device, under a lock); make that first call before any stream capture
- * begins.  Every call on a device shares the one array: each call zeroes what
+ * Every call looks up the array's device address on the current device
+ * afresh, so a cudaDeviceReset or a re-created context between calls is
+ * safe.  The first call on a device may load the library's device code;
+ * make it before any stream capture begins: a first call made while
+ * `stream` is capturing returns MASKLLM_ERR_INVALID_ARG and launches
+ * nothing.  Every call on a device shares the one array: each call zeroes what
  * must start at zero and overwrites the rest, so nothing carries over from
  * the previous call, but calls that overlap on the GPU (other streams, other
  * host threads) race on the array and give wrong results.  Issue them in

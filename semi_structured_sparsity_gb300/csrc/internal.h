@@ -20,25 +20,10 @@ struct RngArgs {
   uint32_t tensor_id;
 };
 
-cudaError_t launch_prior_init(const Device& d, const uint16_t* W, int64_t rows, int64_t cols,
-                              float scale, float* logits, cudaStream_t s);
-cudaError_t launch_forward(const Device& d, const uint16_t* W, const float* logits, int64_t rows,
-                           int64_t cols, float tau, float kappa, RngArgs rng, uint16_t* W_out,
-                           float* row_sq, float* probs, cudaStream_t s);
-cudaError_t launch_backward(const Device& d, const uint16_t* W, const float* logits,
-                            const uint16_t* G, int64_t rows, int64_t cols, float tau, float kappa,
-                            RngArgs rng, float reg_coeff, float* dlogits, cudaStream_t s);
-cudaError_t launch_hard_compress(const Device& d, const uint16_t* W, const float* logits,
-                                 int64_t rows, int64_t cols, uint16_t* values, uint32_t* meta,
-                                 uint8_t* idx, cudaStream_t s);
 cudaError_t launch_decompress(const Device& d, const uint16_t* values, const uint32_t* meta,
                               int64_t rows, int64_t cols, uint16_t* W_out, cudaStream_t s);
 cudaError_t launch_noise_words(const Device& d, RngArgs rng, int64_t group_begin, int64_t n,
                                uint32_t* out4, cudaStream_t s);
-
-// Reads the device error word of the current device on stream s (waiting for
-// s), then clears it.
-cudaError_t read_and_clear_error_word(cudaStream_t s, uint32_t* value);
 
 // ---- pipelined streaming kernels (kernels_stream.cu) ----------------------
 

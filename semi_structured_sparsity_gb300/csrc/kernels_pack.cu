@@ -1,96 +1,20 @@
-// kernels_pack.cu -- hard mask extraction, 2:4 compression and its inverse,
-// and the noise-word export.
+// kernels_pack.cu -- the inverse of 2:4 compression, logits from a given
+// mask, and the noise-word export.
 //
-// "MaskLLM: Learnable Semi-Structured Sparsity for Large Language Models":
-// the mask that is deployed is the learned distribution's most likely
-// candidate.  "Accelerating Sparse Deep Neural Networks", Sec. 3.1: a 2:4
-// matrix is stored as the two kept values of each group of four plus 2 bits
-// per kept value giving its position; the constant sparsity of every group
-// means fixed offsets and no data-dependent indirection.
+// "Accelerating Sparse Deep Neural Networks", Sec. 3.1: a 2:4 matrix is
+// stored as the two kept values of each group of four plus 2 bits per kept
+// value giving its position; the constant sparsity of every group means
+// fixed offsets and no data-dependent indirection.  (The compression itself
+// is a streaming kernel, kernels_stream.cu.)
 //
-// One work item is 8 groups = 32 weights = one 32-bit metadata word:
-// 64 bytes of W and 192 bytes of logits in, 32 bytes of values and 4 bytes
-// of metadata out (9.125 bytes per weight).
+// Decompression: one work item is 8 groups = 32 weights = one 32-bit
+// metadata word: 32 bytes of values and 4 bytes of metadata in, 64 bytes of
+// W out.
 #include "device_common.cuh"
 #include "internal.h"
 
 namespace maskllm {
 namespace {
-
-// Candidate c's kept positions (i, j) and metadata code i | j << 2, packed one
-// nibble per candidate: c0 (0,1) c1 (0,2) c2 (0,3) c3 (1,2) c4 (1,3) c5 (2,3).
-constexpr uint32_t kPairI = 0x211000u;
-constexpr uint32_t kPairJ = 0x332321u;
-constexpr uint32_t kCode = 0xED9C84u;
-
-// argmax over the raw logits: the first maximum wins; a NaN never wins; six
-// NaNs select candidate 0.
-__device__ __forceinline__ int hard_index(const float L[kCand]) {
-  int best = 0;
-  float bv = L[0];
-  bool bnan = isnan(L[0]);
-#pragma unroll
-  for (int c = 1; c < kCand; ++c) {
-    if (!isnan(L[c]) && (bnan || L[c] > bv)) {
-      best = c;
-      bv = L[c];
-      bnan = false;
-    }
-  }
-  return best;
-}
-
-__device__ __forceinline__ uint32_t pick(uint32_t e0, uint32_t e1, uint32_t e2, uint32_t e3,
-                                         uint32_t k) {
-  return k == 0 ? e0 : (k == 1 ? e1 : (k == 2 ? e2 : e3));
-}
-
-__global__ void __launch_bounds__(256) hard_compress_kernel(
-    const uint4* __restrict__ W, const float4* __restrict__ L, uint4* __restrict__ vals,
-    uint32_t* __restrict__ meta, uint2* __restrict__ idx, int64_t items) {
-  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < items;
-       q += (int64_t)gridDim.x * blockDim.x) {
-    uint32_t wd[16];
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const uint4 w = __ldcs(W + 4 * q + v);
-      wd[4 * v + 0] = w.x;
-      wd[4 * v + 1] = w.y;
-      wd[4 * v + 2] = w.z;
-      wd[4 * v + 3] = w.w;
-    }
-    float lg[8 * kCand];
-#pragma unroll
-    for (int v = 0; v < 12; ++v) {
-      const float4 l = __ldcs(L + 12 * q + v);
-      lg[4 * v + 0] = l.x;
-      lg[4 * v + 1] = l.y;
-      lg[4 * v + 2] = l.z;
-      lg[4 * v + 3] = l.w;
-    }
-    uint32_t out[8];
-    uint32_t code_word = 0;
-    uint32_t idx_lo = 0, idx_hi = 0;
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const int c = hard_index(lg + kCand * g);
-      const uint32_t i = (kPairI >> (4 * c)) & 0xFu;
-      const uint32_t j = (kPairJ >> (4 * c)) & 0xFu;
-      const uint32_t e0 = wd[2 * g] & 0xFFFFu, e1 = wd[2 * g] >> 16;
-      const uint32_t e2 = wd[2 * g + 1] & 0xFFFFu, e3 = wd[2 * g + 1] >> 16;
-      out[g] = pick(e0, e1, e2, e3, i) | (pick(e0, e1, e2, e3, j) << 16);
-      code_word |= ((kCode >> (4 * c)) & 0xFu) << (4 * g);
-      if (g < 4)
-        idx_lo |= static_cast<uint32_t>(c) << (8 * g);
-      else
-        idx_hi |= static_cast<uint32_t>(c) << (8 * (g - 4));
-    }
-    __stcs(vals + 2 * q, make_uint4(out[0], out[1], out[2], out[3]));
-    __stcs(vals + 2 * q + 1, make_uint4(out[4], out[5], out[6], out[7]));
-    __stcs(meta + q, code_word);
-    if (idx != nullptr) __stcs(idx + q, make_uint2(idx_lo, idx_hi));
-  }
-}
 
 __global__ void __launch_bounds__(256) decompress_kernel(const uint4* __restrict__ vals,
                                                          const uint32_t* __restrict__ meta,
@@ -189,16 +113,6 @@ int grid_for(int64_t items, int threads, const Device& d, int per_sm) {
 }
 
 }  // namespace
-
-cudaError_t launch_hard_compress(const Device& d, const uint16_t* W, const float* logits,
-                                 int64_t rows, int64_t cols, uint16_t* values, uint32_t* meta,
-                                 uint8_t* idx, cudaStream_t s) {
-  const int64_t items = rows * cols / 32;
-  hard_compress_kernel<<<grid_for(items, 256, d, 8), 256, 0, s>>>(
-      reinterpret_cast<const uint4*>(W), reinterpret_cast<const float4*>(logits),
-      reinterpret_cast<uint4*>(values), meta, reinterpret_cast<uint2*>(idx), items);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_decompress(const Device& d, const uint16_t* values, const uint32_t* meta,
                               int64_t rows, int64_t cols, uint16_t* W_out, cudaStream_t s) {

@@ -32,6 +32,8 @@
 //   * Every wait is bounded (pipeline.cuh).  On a timeout the CTA raises an
 //     abort flag, sets the device error word, the producer waits (bounded)
 //     for its copies still in flight, and all warps return.
+#include <atomic>
+
 #include "device_common.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
@@ -940,8 +942,10 @@ __global__ void __launch_bounds__(Op::kThreads, 1)
 // Host side.
 // ---------------------------------------------------------------------------
 
-uint64_t g_wait_ns = 2000000000ull;   // 2 s
-int g_withhold_loads = 0;
+// Host settings, written by the exported setters from any thread and read
+// by every launch.
+std::atomic<uint64_t> g_wait_ns{2000000000ull};   // 2 s
+std::atomic<int> g_withhold_loads{0};
 
 void describe(StreamParams& p, const StreamMatrix* mats, int n) {
   p.nmats = n;
@@ -975,9 +979,10 @@ void describe(StreamParams& p, const StreamMatrix* mats, int n) {
   }
   p.total_units = units;
   p.total_chunks = chunks;
-  p.wait_ns = g_wait_ns;
-  p.drain_ns = g_wait_ns > 1000000000ull ? g_wait_ns : 1000000000ull;
-  p.withhold_loads = g_withhold_loads;
+  const uint64_t wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  p.wait_ns = wait_ns;
+  p.drain_ns = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
+  p.withhold_loads = g_withhold_loads.load(std::memory_order_relaxed);
 }
 
 template <class Op>
@@ -1062,9 +1067,11 @@ cudaError_t stream_forward_stats(const Device& d, const StreamMatrix* m, int n, 
   return launch<FwdStatsOp<kGPT>>(d, p, s);
 }
 
-void stream_set_wait_ns(uint64_t ns) { g_wait_ns = ns; }
-uint64_t stream_wait_ns() { return g_wait_ns; }
-void stream_set_withhold_loads(int on) { g_withhold_loads = on; }
+void stream_set_wait_ns(uint64_t ns) { g_wait_ns.store(ns, std::memory_order_relaxed); }
+uint64_t stream_wait_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+void stream_set_withhold_loads(int on) {
+  g_withhold_loads.store(on, std::memory_order_relaxed);
+}
 
 cudaError_t read_and_clear_stream_error(cudaStream_t s, uint32_t* value) {
   uint32_t zero = 0;

@@ -1,19 +1,15 @@
 // maskllm_api.cu -- the C ABI declared in include/maskllm.h: argument
 // validation on the host, then kernel launches on the caller's stream.
 //
-// Kernels: the pipelined streaming kernels (kernels_stream.cu) serve every
-// call.  Setting MASKLLM_KERNELS=direct in the environment selects the
-// per-matrix kernels with direct vector loads instead (kernels_mask.cu,
-// kernels_pack.cu); both compute the same results and exist side by side so
-// their throughput can be compared on the same build.
+// Kernels: the pipelined streaming kernels (kernels_stream.cu) serve the
+// prior, forward, backward, hard-compress and diagnostics calls; the others
+// live in kernels_pack.cu, kernels_perm.cu and kernels_spmm.cu.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
-#include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "internal.h"
 #include "maskllm.h"
@@ -32,14 +28,6 @@ maskllm_status cuda_fail(cudaError_t e) {
   strncpy(t_last_cuda_error, msg ? msg : "unknown CUDA error", sizeof(t_last_cuda_error) - 1);
   t_last_cuda_error[sizeof(t_last_cuda_error) - 1] = '\0';
   return MASKLLM_ERR_CUDA;
-}
-
-bool use_direct_kernels() {
-  static const bool direct = [] {
-    const char* v = getenv("MASKLLM_KERNELS");
-    return v != nullptr && strcmp(v, "direct") == 0;
-  }();
-  return direct;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -197,23 +185,6 @@ StreamMatrix to_stream(const maskllm_matrix& m, Op op) {
   return s;
 }
 
-cudaError_t run_direct(const Device& d, const Call& c, const maskllm_matrix& m, cudaStream_t s) {
-  const RngArgs rng{c.seed, c.step, m.tensor_id};
-  switch (c.op) {
-    case Op::kPrior: return launch_prior_init(d, m.W, m.rows, m.cols, c.scale, m.logits_out, s);
-    case Op::kForward:
-      return launch_forward(d, m.W, m.logits, m.rows, m.cols, c.tau, c.kappa, rng, m.W_out,
-                            m.row_sq_out, m.probs_out, s);
-    case Op::kBackward:
-      return launch_backward(d, m.W, m.logits, m.grad_W_out, m.rows, m.cols, c.tau, c.kappa, rng,
-                             c.reg, m.dlogits_out, s);
-    case Op::kCompress:
-      return launch_hard_compress(d, m.W, m.logits, m.rows, m.cols, m.values_out, m.meta_out,
-                                  m.idx_out, s);
-  }
-  return cudaErrorInvalidValue;
-}
-
 maskllm_status run(const Call& c, const maskllm_matrix* mats, int32_t n, cudaStream_t s) {
   if (mats == nullptr || n < 1) return MASKLLM_ERR_INVALID_ARG;
   if (c.op == Op::kForward || c.op == Op::kBackward) MK_TRY(check_temperature(c.tau, c.kappa));
@@ -264,11 +235,6 @@ maskllm_status run(const Call& c, const maskllm_matrix* mats, int32_t n, cudaStr
   Device d;
   cudaError_t e = current_device(&d);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (use_direct_kernels()) {
-    for (int32_t i = 0; i < n; ++i)
-      if ((e = run_direct(d, c, mats[i], s)) != cudaSuccess) return cuda_fail(e);
-    return MASKLLM_OK;
-  }
   for (int32_t b = 0; b < n; b += kMaxBatch) {
     const int32_t nb = n - b < kMaxBatch ? n - b : kMaxBatch;
     StreamMatrix sm[kMaxBatch];
@@ -697,14 +663,12 @@ maskllm_status maskllm_test_spmm_tile_n(int32_t n) {
 }
 
 maskllm_status maskllm_device_status(maskllm_stream_t stream) {
-  uint32_t a = 0, b = 0, c = 0;
-  cudaError_t e = maskllm::read_and_clear_error_word(stream, &a);
-  if (e == cudaSuccess) e = maskllm::read_and_clear_stream_error(stream, &b);
-  uint32_t g = 0;
+  uint32_t b = 0, c = 0, g = 0;
+  cudaError_t e = maskllm::read_and_clear_stream_error(stream, &b);
   if (e == cudaSuccess) e = maskllm::read_and_clear_perm_error(stream, &c);
   if (e == cudaSuccess) e = maskllm::read_and_clear_spmm_error(stream, &g);
   if (e != cudaSuccess) return maskllm::cuda_fail(e);
-  if ((a | b | g) != 0) return MASKLLM_ERR_TIMEOUT;
+  if ((b | g) != 0) return MASKLLM_ERR_TIMEOUT;
   return c != 0 ? MASKLLM_ERR_INVALID_ARG : MASKLLM_OK;
 }
 
@@ -759,23 +723,30 @@ static __device__ __align__(256) unsigned char
 
 namespace {
 
-std::mutex g_perm_static_mutex;
-void* g_perm_static_addr[kMaxDevices];   // the array's device address, per device
+// Devices on which a lookup of the array's address has succeeded once.
+std::atomic<bool> g_perm_static_seen[kMaxDevices];
 
-// Device address of the array on device `dev` (the current device): looked
-// up once per device.  In host code the array's name is only a host-side
-// stand-in, never an address a kernel may use.
-cudaError_t perm_static_scratch(int dev, void** addr) {
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_perm_static_mutex);
-  if (g_perm_static_addr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_perm_static_scratch);
-    if (e != cudaSuccess) return e;
-    g_perm_static_addr[dev] = p;
+// Device address of the array on the current device `dev`.  In host code the
+// array's name is only a host-side stand-in, never an address a kernel may
+// use.  The address is looked up on every call (a lookup allocates nothing):
+// after cudaDeviceReset, or with another context current, the module may sit
+// elsewhere, and a remembered address would point at memory that is not the
+// array.  The first lookup on a device may load the module, which must not
+// happen inside a stream capture: that case is refused before any lookup.
+maskllm_status perm_static_scratch(int dev, cudaStream_t s, void** addr) {
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
+  if (!g_perm_static_seen[dev].load(std::memory_order_acquire)) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (cap != cudaStreamCaptureStatusNone) return MASKLLM_ERR_INVALID_ARG;
   }
-  *addr = g_perm_static_addr[dev];
-  return cudaSuccess;
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_perm_static_scratch);
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_perm_static_seen[dev].store(true, std::memory_order_release);
+  *addr = p;
+  return MASKLLM_OK;
 }
 
 }  // namespace
@@ -808,8 +779,7 @@ extern "C" maskllm_status maskllm_perm_search_static(const uint16_t* W, int64_t 
   cudaError_t e = maskllm::current_device(&d);
   if (e != cudaSuccess) return maskllm::cuda_fail(e);
   void* scratch = nullptr;
-  e = maskllm::perm_static_scratch(d.ordinal, &scratch);
-  if (e != cudaSuccess) return maskllm::cuda_fail(e);
+  MK_TRY(maskllm::perm_static_scratch(d.ordinal, stream, &scratch));
   return maskllm::finish(maskllm::perm_search(d, W, rows, cols, perm, max_swaps, scratch,
                                               swaps_out, gains_out, n_swaps_out, shift_out,
                                               stream));

@@ -9,6 +9,10 @@ call, although every call reuses the same array.  This file is collected
 last so that a run stopping at the first failure has run every other test.
 """
 
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -17,6 +21,7 @@ from semi_structured_sparsity_gb300 import binding as mk
 from semi_structured_sparsity_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -82,3 +87,62 @@ def test_static_scratch_rejects_shapes_beyond_its_size():
     assert st == 2    # MASKLLM_ERR_SHAPE
     assert mk.maskllm_perm_workspace_bytes(3584, 1024) > mk.PERM_SEARCH_STATIC_BYTES
     assert mk.maskllm_perm_workspace_bytes(3583, 1024) <= mk.PERM_SEARCH_STATIC_BYTES
+
+
+def test_static_scratch_call_allocates_no_device_memory():
+    """The property the entry point exists for: with its outputs made
+    beforehand, a call leaves the device's free memory as it was (a first
+    call has loaded the library's device code)."""
+    L = mk.lib()
+    Wt, p = _case(512, 1024, 15)
+    swaps = torch.zeros((40, 2), dtype=torch.int32, device="cuda")
+    gains = torch.zeros((40,), dtype=torch.int64, device="cuda")
+    small = torch.zeros((8,), dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call(perm):
+        st = L.maskllm_perm_search_static(Wt.data_ptr(), 512, 1024, perm.data_ptr(), 40,
+                                          swaps.data_ptr(), gains.data_ptr(), small.data_ptr(),
+                                          small.data_ptr() + 16, s)
+        assert st == 0, mk.maskllm_status_string(st)
+        torch.cuda.synchronize()
+
+    first, second = p.clone(), p.clone()
+    call(first)
+    free_before = torch.cuda.mem_get_info()[0]
+    call(second)
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert torch.equal(first, second)
+
+
+_CAPTURE_SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r})
+import torch
+from semi_structured_sparsity_gb300 import binding as mk
+from semi_structured_sparsity_gb300 import workloads as W
+L = mk.lib()
+Wt = W.normal_bf16(64, 256, 0.02, 16, device="cuda")
+perm = torch.arange(256, dtype=torch.int32, device="cuda")
+small = torch.zeros((8,), dtype=torch.int32, device="cuda")
+side = torch.cuda.Stream()
+graph = torch.cuda.CUDAGraph()
+with torch.cuda.graph(graph, stream=side):
+    st = L.maskllm_perm_search_static(Wt.data_ptr(), 64, 256, perm.data_ptr(), 4, None, None,
+                                      small.data_ptr(), None, side.cuda_stream)
+print("status", st)
+st2 = L.maskllm_perm_search_static(Wt.data_ptr(), 64, 256, perm.data_ptr(), 4, None, None,
+                                   small.data_ptr(), None, torch.cuda.current_stream().cuda_stream)
+torch.cuda.synchronize()
+print("after", st2)
+"""
+
+
+def test_static_scratch_first_call_inside_a_capture_is_refused():
+    """In a fresh process, a first call made while its stream is being
+    captured returns MASKLLM_ERR_INVALID_ARG without launching; the next call
+    outside the capture works."""
+    r = subprocess.run([sys.executable, "-c", _CAPTURE_SCRIPT.format(root=ROOT)],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-3000:]
+    assert "status 1" in r.stdout and "after 0" in r.stdout, r.stdout
