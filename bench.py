@@ -51,6 +51,9 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other weight sets (full LLaMA-2-7B, Nemotron-4-15B layers, "
+                         "near-one-hot compress)")
     ap.add_argument("--spmm-tile-n", type=int, default=0,
                     help="force the sparse product's tile width (128..256, a multiple of 32) "
                          "for the spmm extra; 0 = the width the library picks per call")
@@ -344,18 +347,25 @@ def run_gpu(args):
     # the dominant kernel's algorithmic bytes over its CUDA-event time (one
     # batched launch per step covers the whole block)
     ach = BYTES_PER_WEIGHT[dominant] * blk.weights / per_kernel_s[dominant] / 1e9
+    # ncu DRAM bytes per launch (read + write) of each kernel, valid only for
+    # the kernel source they were captured on
     tt = traffic_table()
     digest = kernel_source_digest()
-    traffic = None
     shape_key = "%s" % args.workload
-    if (dominant, shape_key) in tt and tt[(dominant, shape_key)][1] == digest:
-        traffic = tt[(dominant, shape_key)][0]
+    for k in KERNELS:
+        hit = tt.get((k, shape_key))
+        kernels[k]["traffic"] = hit[0] if hit is not None and hit[1] == digest else None
+        kernels[k]["algorithmic_bytes"] = BYTES_PER_WEIGHT[k] * blk.weights
+    traffic = kernels[dominant]["traffic"]
 
     extras = run_extras(blk, peak, dev, spmm_tile_n=args.spmm_tile_n)
 
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, blk, ranks, dev, only=only)
+
+    if not args.no_configs and ranks.world == 1 and not args.only:
+        extras["configs"] = run_configs(dev, peak)
 
     cpu = None
     if not args.no_cpu_baseline and ranks.rank == 0 and ranks.world == 1:
@@ -589,6 +599,144 @@ def run_perm_search(blk, dev, steps=256, reps=3):
             "kept_magnitude_gain": round((m_end - m_start) / max(m_start, 1), 6),
             "note": "evals = cols^2 * rows max-and-add; table_build includes the scan and "
                     "set-up kernels"}
+
+
+def _config_block(wl, layer, dev, outputs):
+    """Resident inputs and the requested outputs of one layer of workload wl
+    (logits built as the step builds them); matrix descriptors for the
+    batched calls."""
+    import torch
+
+    from semi_structured_sparsity_gb300 import binding as mk
+    from semi_structured_sparsity_gb300 import workloads as W
+    mats = []
+    for m in range(len(wl.matrices)):
+        x = W.matrix_inputs(wl, layer, m, device=dev, with_grad="backward" in outputs)
+        if x.L is None:
+            x.L = mk.maskllm_prior_init(x.W, wl.prior_scale) + x.L_noise
+            x.L_noise = None
+        r, c = x.rows, x.cols
+        d = {"W": x.W, "logits": x.L, "grad_W_out": x.G, "tensor_id": x.tensor_id}
+        if "forward" in outputs:
+            d["W_out"] = torch.empty_like(x.W)
+            d["row_sq_out"] = torch.empty((r,), dtype=torch.float32, device=dev)
+        if "backward" in outputs:
+            d["dlogits_out"] = torch.empty_like(x.L)
+        if "hard_compress" in outputs:
+            d["values_out"] = torch.empty((r, c // 2), dtype=torch.bfloat16, device=dev)
+            d["meta_out"] = torch.empty((r, c // 32), dtype=torch.int32, device=dev)
+        mats.append(d)
+    return mats
+
+
+def _timed_calls(fn, dev, reps):
+    """Mean seconds of one fn() over `reps` back-to-back calls (after one
+    untimed call), CUDA events on the current stream."""
+    import torch
+    fn()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / 1e3 / reps
+
+
+def _kernel_line(weights, seconds, op, peak, launches):
+    gbs = BYTES_PER_WEIGHT[op] * weights / seconds / 1e9
+    return {"us": round(seconds * 1e6, 1), "weights_per_s": weights / seconds,
+            "GB_per_s": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
+            "launches": launches}
+
+
+def run_configs(dev, peak, reps=5):
+    """The other weight sets of the mask layer, CUDA-event timed on this GPU
+    (each config's buffers are freed before the next):
+      * llama2_7b_full: one forward and one backward mask step over all 32
+        layers x 7 matrices (6,476,005,376 weights) with every layer's logits
+        and dlogits resident (tau 0.5), as batched calls of 16 matrices;
+      * nemotron4_15b: forward and backward of each of the 32 layers (6
+        matrices, 390,070,272 weights per layer), layer by layer, each
+        layer's inputs generated, timed and freed in turn (tau 0.2, kappa 500);
+      * compress_7b: hard mask + 2:4 compression of the LLaMA-2-7B block
+        with near-one-hot logits and 1% exact ties."""
+    import torch
+
+    from semi_structured_sparsity_gb300 import binding as mk
+    from semi_structured_sparsity_gb300 import workloads as W
+    L = mk.lib()
+    s = torch.cuda.current_stream(dev).cuda_stream
+    out = {}
+
+    def batched(op, wl, arr, n):
+        if op == "forward":
+            st = L.maskllm_forward_batched(arr, n, wl.tau, wl.kappa, 0, 0, s)
+        elif op == "backward":
+            st = L.maskllm_backward_batched(arr, n, wl.tau, wl.kappa, 0, 0, 0.0, s)
+        else:
+            st = L.maskllm_hard_compress_batched(arr, n, s)
+        if st != 0:
+            raise mk.MaskLLMError("maskllm_%s_batched" % op, st)
+
+    # config 3: the full model, all layers resident
+    wl = W.WORKLOADS["llama2_7b_full"]
+    mats = [d for layer in range(wl.layers)
+            for d in _config_block(wl, layer, dev, ("forward", "backward"))]
+    torch.cuda.synchronize(dev)
+    arr = mk.matrix_array(mats)
+    weights = sum(d["W"].numel() for d in mats)
+    launches = (len(mats) + mk.MAX_BATCH - 1) // mk.MAX_BATCH
+    k3 = {op: _kernel_line(weights, _timed_calls(lambda: batched(op, wl, arr, len(mats)), dev,
+                                                 reps), op, peak, launches)
+          for op in ("forward", "backward")}
+    step = sum(v["us"] for v in k3.values()) / 1e6
+    out["llama2_7b_full"] = {"weights": weights, "matrices": len(mats), "tau": wl.tau,
+                             "kappa": wl.kappa, "kernels": k3,
+                             "step_ms": round(step * 1e3, 3), "weights_per_s": weights / step,
+                             "resident_GB": round(sum(t.numel() * t.element_size()
+                                                      for d in mats for t in d.values()
+                                                      if torch.is_tensor(t)) / 1e9, 1)}
+    del mats, arr
+    torch.cuda.empty_cache()
+
+    # config 4: Nemotron-4-15B shapes, 32 layers one at a time
+    wl = W.WORKLOADS["nemotron4_15b"]
+    tot = {"forward": 0.0, "backward": 0.0}
+    weights = 0
+    launches = 0
+    for layer in range(wl.layers):
+        mats = _config_block(wl, layer, dev, ("forward", "backward"))
+        torch.cuda.synchronize(dev)
+        arr = mk.matrix_array(mats)
+        for op in tot:
+            tot[op] += _timed_calls(lambda: batched(op, wl, arr, len(mats)), dev, 2)
+        weights += sum(d["W"].numel() for d in mats)
+        launches += 1
+        del mats, arr
+    torch.cuda.empty_cache()
+    k4 = {op: _kernel_line(weights, sec, op, peak, launches) for op, sec in tot.items()}
+    step = sum(tot.values())
+    out["nemotron4_15b"] = {"weights": weights, "layers": wl.layers, "tau": wl.tau,
+                            "kappa": wl.kappa, "kernels": k4,
+                            "step_ms": round(step * 1e3, 3), "weights_per_s": weights / step,
+                            "note": "per-kernel time summed over the 32 layers (one batched "
+                                    "launch per layer and kernel)"}
+
+    # config 5: hard mask + compression of near-one-hot logits with ties
+    wl = W.WORKLOADS["compress_7b"]
+    mats = _config_block(wl, 0, dev, ("hard_compress",))
+    torch.cuda.synchronize(dev)
+    arr = mk.matrix_array(mats)
+    weights = sum(d["W"].numel() for d in mats)
+    sec = _timed_calls(lambda: batched("hard_compress", wl, arr, len(mats)), dev, 20)
+    out["compress_7b"] = {"weights": weights, "kernels": {
+        "hard_compress": _kernel_line(weights, sec, "hard_compress", peak, 1)}}
+    del mats, arr
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, blk, ranks, dev, only=None):

@@ -283,6 +283,11 @@ struct OpBase {
   // in its lane 0's slot and the producer adds kConsumerWarps values; else
   // every thread leaves its own partial and the producer adds kConsumers
   static constexpr bool kWarpRowSums = false;
+  static constexpr int kIntQuantity = -1;   // row quantity summed as an integer (none)
+  // the consumers write row partials into bytes the next copy overwrites
+  // (their consumed W slots): the producer orders those generic-proxy
+  // accesses before its async-proxy copies with a proxy fence
+  static constexpr bool kPartialsInCopyTarget = false;
 };
 
 template <int GPT>
@@ -526,6 +531,30 @@ struct CompressOp : OpBase<GPT, 4> {
   }
 };
 
+// The previous step's draws of a chunk (one byte per group) travel with the
+// chunk's other inputs as one more bulk copy when the copy's start and size
+// are 16-byte multiples (every chunk of rows whose length is a multiple of
+// 64 weights); otherwise each consumer thread loads its two bytes directly.
+__device__ __forceinline__ bool prev_staged(const MatDesc& d, const Chunk& c) {
+  return d.G != nullptr && ((c.g0 | c.ng) & 15) == 0;
+}
+
+__device__ __forceinline__ void issue_prev(const MatDesc& d, const Chunk& c, uint8_t* dst,
+                                           uint64_t* bar) {
+  if (prev_staged(d, c)) {
+    mbar_expect_tx(bar, static_cast<uint32_t>(c.ng));
+    bulk_load(dst, static_cast<const uint8_t*>(d.G) + c.g0, static_cast<uint32_t>(c.ng), bar);
+  }
+}
+
+// This thread's previous draws (two bytes: groups 2t, 2t + 1).
+__device__ __forceinline__ uint32_t load_prev2(const MatDesc& d, const Chunk& c,
+                                               const uint8_t* staged, int t) {
+  if (d.G == nullptr) return 0u;
+  if (prev_staged(d, c)) return *reinterpret_cast<const uint16_t*>(staged + 2 * t);
+  return static_cast<const uint16_t*>(d.G)[c.g0 / 2 + t];
+}
+
 // Convergence diagnostics ("MaskLLM" project page, Fig. 5): per step, the
 // candidate drawn for every group (the first maximum of the noisy logits z,
 // the mask the soft mask tends to as tau -> 0), the L1 distance of the drawn
@@ -542,11 +571,15 @@ struct StatsOp : OpBase<GPT, 4> {
   static constexpr bool kRefillFirst = true;   // partials after the logits
   static constexpr uint32_t kOutOffset = 0;
   static constexpr uint32_t kOutBytesPerGroup = 0;
-  // logits, then two per-thread partials (L1 distance, max probability)
+  // logits, per-thread partials (L1 distance, max probability), then the
+  // previous draws (one byte per group)
   static constexpr int kRowQuantities = 2;
+  static constexpr bool kWarpRowSums = true;
+  static constexpr int kIntQuantity = 0;   // the L1 distance is an integer count
   static constexpr uint32_t kPartOffset = kChunkGroups * 24;
   static constexpr uint32_t kPartStride = 8;
-  static constexpr uint32_t kStageBytes = kPartOffset + (kChunkGroups / GPT) * kPartStride;
+  static constexpr uint32_t kPrevOffset = kPartOffset + (kChunkGroups / GPT) * kPartStride;
+  static constexpr uint32_t kStageBytes = kPrevOffset + kChunkGroups;
 
   __device__ static bool want_row(const MatDesc& d, int q) {
     return q == 0 ? (d.out1 != nullptr && d.G != nullptr) : d.out2 != nullptr;
@@ -562,20 +595,16 @@ struct StatsOp : OpBase<GPT, 4> {
     const uint32_t lb = static_cast<uint32_t>(c.ng) * 24;
     mbar_expect_tx(bar, lb);
     bulk_load(st, static_cast<const uint8_t*>(d.L) + c.g0 * 24, lb, bar);
+    issue_prev(d, c, st + kPrevOffset, bar);
   }
 
   __device__ static void consume(const StreamParams& p, const MatDesc& d, const Chunk& c,
                                  uint8_t* st, int t, const float* tab, float* acc) {
+    static_assert(GPT == 2, "draws are stored as one 16-bit pair per thread");
     float L[6 * GPT];
     load_l<GPT>(st, t, L);
     const int64_t unit = c.g0 / GPT + t;
-    uint32_t prev = 0;
-    if (d.G != nullptr) {
-      if constexpr (GPT == 2)
-        prev = static_cast<const uint16_t*>(d.G)[unit];
-      else
-        prev = static_cast<const uint8_t*>(d.G)[unit];
-    }
+    const uint32_t prev = load_prev2(d, c, st + kPrevOffset, t);
     uint32_t drawn = 0;
     const uint64_t g0 = static_cast<uint64_t>(c.g0) + static_cast<uint64_t>(GPT * t);
 #pragma unroll
@@ -600,12 +629,7 @@ struct StatsOp : OpBase<GPT, 4> {
       for (int c6 = 0; c6 < kCand; ++c6) sum += ex2_approx((y[c6] - m) * kLog2e);
       acc[1] += rcp_approx(sum);   // the largest term is 2^0 = 1
     }
-    if (d.out0 != nullptr) {
-      if constexpr (GPT == 2)
-        static_cast<uint16_t*>(d.out0)[unit] = static_cast<uint16_t>(drawn);
-      else
-        static_cast<uint8_t*>(d.out0)[unit] = static_cast<uint8_t>(drawn);
-    }
+    if (d.out0 != nullptr) static_cast<uint16_t*>(d.out0)[unit] = static_cast<uint16_t>(drawn);
   }
 };
 
@@ -615,8 +639,7 @@ struct StatsOp : OpBase<GPT, 4> {
 // scaled logits fl32(kappa * L) it forms on the way give the distribution's
 // largest probability.  W' and row_sq are computed exactly as in FwdOp; the
 // draws, L1 and max-probability exactly as in StatsOp.  Row quantities: 0
-// row_sq, 1 L1 distance, 2 max-probability sum (three floats in the
-// thread's consumed W slot).
+// row_sq, 1 L1 distance, 2 max-probability sum.
 template <int GPT>
 struct FwdStatsOp : OpBase<GPT, 4> {
   static constexpr bool kTable = true, kStaged = false, kWarpWide = false;
@@ -625,6 +648,7 @@ struct FwdStatsOp : OpBase<GPT, 4> {
   static constexpr uint32_t kPartOffset = 0;
   static constexpr uint32_t kPartStride = 8 * GPT;
   static_assert(8 * GPT >= 12, "three row partials fit the thread's W slot");
+  static constexpr bool kPartialsInCopyTarget = true;
   __device__ static bool want_row(const MatDesc& d, int q) {
     return q == 0 ? d.out1 != nullptr : (q == 1 ? (d.out3 != nullptr && d.G != nullptr)
                                                  : d.out4 != nullptr);
@@ -801,6 +825,7 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
       // a staged store may still be reading this stage's output region:
       // wait before the refill if the copies land there, after it if not
       if (Op::kStaged && Op::kOutOverlapsInput) bulk_wait_reads();
+      if (Op::kPartialsInCopyTarget) fence_proxy_async_smem();
       if (!p.withhold_loads)
         Op::issue(p.mats[c.mat], c, stages + s * Op::kStageBytes, &full[s]);
       else
@@ -888,7 +913,12 @@ __device__ void consumer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
               reinterpret_cast<float*>(st + Op::kPartOffset + (t & ~31) * Op::kPartStride);
 #pragma unroll
           for (int q = 0; q < Op::kRowQuantities; ++q) {
-            const float v = warp_sum(acc[q]);
+            // an integer count below 2^24 is exact in fp32 and sums in one
+            // warp-reduce instruction
+            const float v = q == Op::kIntQuantity
+                                ? static_cast<float>(__reduce_add_sync(
+                                      0xFFFFFFFFu, static_cast<uint32_t>(acc[q])))
+                                : warp_sum(acc[q]);
             if (lane == 0) part[q] = v;
             acc[q] = 0.f;
           }
