@@ -33,6 +33,7 @@
 //     abort flag, sets the device error word, the producer waits (bounded)
 //     for its copies still in flight, and all warps return.
 #include <atomic>
+#include <cstddef>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -63,12 +64,13 @@ struct MatDesc {
   void* out2;             // forward: probs; compress: idx; forward + stats: draws
   void* out3;             // forward + stats: L1 per row
   void* out4;             // forward + stats: max-probability sum per row
-  int64_t rows;
+  int64_t rows;           // rows; flat chunking: chunks
   int64_t unit_begin;     // first unit of this matrix in the launch's unit list
   int64_t chunk_begin;    // first chunk of this matrix in the launch's chunk list
   int32_t gpr;            // groups per row (cols / 4)
   int32_t cpr;            // chunks per row when a row spans >= 1 chunk, else 0
-  int32_t rpc;            // rows per chunk when rows are short, else 0
+  int32_t rpc;            // rows per chunk when rows are short, else 0; flat
+                          // chunking: the groups of the last chunk
   uint32_t tensor_id;
 };
 
@@ -91,7 +93,15 @@ struct StreamParams {
   uint64_t drain_ns;       // bound of the final wait for copies in flight
   int32_t withhold_loads;  // test hook: no copies are issued
   Scalars s;
+  int32_t flat;            // the matrices are chunked flat (must equal Op::kFlat)
 };
+
+// Where the Philox round keys sit in the parameter block matters: with the
+// keys on an 8-byte boundary the forward measured 2% slower (376 -> 384 us
+// on the LLaMA-2-7B block) and the fused diagnostics 3% slower, the same
+// code otherwise.  New fields go after `s`.
+static_assert(offsetof(StreamParams, s) % 8 == 4 && offsetof(Scalars, keys) % 8 == 0,
+              "round keys at 4 mod 8 in the parameter block");
 
 struct Chunk {
   int32_t mat;
@@ -105,7 +115,10 @@ __device__ __forceinline__ int64_t units_of(const MatDesc& d) {
   return d.cpr > 0 ? d.rows : (d.rows + d.rpc - 1) / d.rpc;
 }
 
-// Walks the chunks of units [u, u_end) of the launch's unit list.
+// Walks the chunks of units [u, u_end) of the launch's unit list.  kFlat:
+// the matrices are chunked flat (describe()), so a matrix's last chunk may
+// be ragged.
+template <bool kFlat>
 struct ChunkIter {
   const StreamParams* p;
   int32_t m;
@@ -129,8 +142,12 @@ struct ChunkIter {
     if (d.cpr > 0) {
       c.row0 = lu;
       c.g0 = lu * d.gpr + static_cast<int64_t>(j) * kChunkGroups;
-      const int64_t rest = d.gpr - static_cast<int64_t>(j) * kChunkGroups;
-      c.ng = static_cast<int32_t>(rest < kChunkGroups ? rest : kChunkGroups);
+      if constexpr (kFlat) {
+        c.ng = lu + 1 == d.rows ? d.rpc : kChunkGroups;   // a ragged last chunk
+      } else {
+        const int64_t rest = d.gpr - static_cast<int64_t>(j) * kChunkGroups;   // of the row
+        c.ng = static_cast<int32_t>(rest < kChunkGroups ? rest : kChunkGroups);
+      }
       const bool last = (j + 1 == d.cpr);
       c.nrows = last ? 1 : 0;
       if (last) {
@@ -288,10 +305,13 @@ struct OpBase {
   // (their consumed W slots): the producer orders those generic-proxy
   // accesses before its async-proxy copies with a proxy fence
   static constexpr bool kPartialsInCopyTarget = false;
+  // chunk the matrices flat (no per-row sums: prior, backward, compress)
+  static constexpr bool kFlat = false;
 };
 
 template <int GPT>
 struct PriorOp : OpBase<GPT, 4> {
+  static constexpr bool kFlat = true;
   static constexpr bool kTable = false, kStaged = true, kWarpWide = false;
   static constexpr bool kOutOverlapsInput = false;   // W in, logits out: separate regions
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
@@ -396,6 +416,7 @@ struct FwdOp : OpBase<GPT, 4> {
 
 template <bool kReg, int GPT>
 struct BwdOp : OpBase<GPT, 4> {
+  static constexpr bool kFlat = true;
   static constexpr bool kTable = true, kStaged = true, kWarpWide = false;
   static constexpr bool kOutOverlapsInput = true;    // dlogits overwrite the logits
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 8 + 24);
@@ -483,6 +504,7 @@ __device__ __forceinline__ uint32_t gather_selector(int c) {
 
 template <int GPT>
 struct CompressOp : OpBase<GPT, 4> {
+  static constexpr bool kFlat = true;
   static constexpr bool kTable = false, kStaged = false, kWarpWide = true;
   static constexpr bool kOutOverlapsInput = false;
   static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
@@ -795,7 +817,7 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
     }
   };
 
-  ChunkIter it;
+  ChunkIter<Op::kFlat> it;
   it.init(&p, u0, u1);
   Chunk c;
   int64_t n = 0;
@@ -977,8 +999,17 @@ __global__ void __launch_bounds__(Op::kThreads, 1)
 std::atomic<uint64_t> g_wait_ns{2000000000ull};   // 2 s
 std::atomic<int> g_withhold_loads{0};
 
-void describe(StreamParams& p, const StreamMatrix* mats, int n) {
+// Chunking of each matrix.  Ops with per-row sums (forward, diagnostics)
+// chunk row by row: a long row is split into chunks, short rows are packed
+// whole, so every row ends inside one chunk range and one CTA.  The other
+// ops (prior, backward, hard-compress) treat the matrix as one flat array of
+// groups (row-major, no padding): chunks of kChunkGroups groups with a
+// ragged last chunk, described as "rows" of one chunk each -- every chunk
+// full, and the CTAs' shares equal to within one chunk whatever the row
+// length.
+void describe(StreamParams& p, const StreamMatrix* mats, int n, bool flat) {
   p.nmats = n;
+  p.flat = flat ? 1 : 0;
   int64_t units = 0, chunks = 0;
   for (int i = 0; i < n; ++i) {
     MatDesc& d = p.mats[i];
@@ -994,7 +1025,13 @@ void describe(StreamParams& p, const StreamMatrix* mats, int n) {
     d.rows = m.rows;
     d.gpr = static_cast<int32_t>(m.cols / 4);
     d.tensor_id = m.tensor_id;
-    if (d.gpr >= kChunkGroups) {
+    if (flat) {
+      const int64_t groups = m.rows * (m.cols / 4);
+      d.gpr = kChunkGroups;
+      d.rows = (groups + kChunkGroups - 1) / kChunkGroups;
+      d.cpr = 1;
+      d.rpc = static_cast<int32_t>(groups - (d.rows - 1) * kChunkGroups);
+    } else if (d.gpr >= kChunkGroups) {
       d.cpr = (d.gpr + kChunkGroups - 1) / kChunkGroups;
       d.rpc = 0;
     } else {
@@ -1017,6 +1054,7 @@ void describe(StreamParams& p, const StreamMatrix* mats, int n) {
 
 template <class Op>
 cudaError_t launch(const Device& dev, const StreamParams& p, cudaStream_t s) {
+  if (p.flat != (Op::kFlat ? 1 : 0)) return cudaErrorInvalidValue;   // chunking mismatch
   const uint32_t bytes = Layout<Op>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(stream_kernel<Op>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -1052,7 +1090,7 @@ static_assert(sizeof(StreamParams) <= 4000, "kernel parameters");
 cudaError_t stream_prior_init(const Device& d, const StreamMatrix* m, int n, float scale,
                               cudaStream_t s) {
   StreamParams p;
-  describe(p, m, n);
+  describe(p, m, n, true);
   p.s = scalars(1.0f, 0.0f, {0, 0, 0}, 0.0f, scale);
   return launch<PriorOp<kGPT>>(d, p, s);
 }
@@ -1060,7 +1098,7 @@ cudaError_t stream_prior_init(const Device& d, const StreamMatrix* m, int n, flo
 cudaError_t stream_forward(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
                            RngArgs rng, bool probs, cudaStream_t s) {
   StreamParams p;
-  describe(p, m, n);
+  describe(p, m, n, false);
   p.s = scalars(tau, kappa, rng, 0.0f, 0.0f);
   return probs ? launch<FwdOp<true, kGPT>>(d, p, s) : launch<FwdOp<false, kGPT>>(d, p, s);
 }
@@ -1068,7 +1106,7 @@ cudaError_t stream_forward(const Device& d, const StreamMatrix* m, int n, float 
 cudaError_t stream_backward(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
                             RngArgs rng, float reg_coeff, cudaStream_t s) {
   StreamParams p;
-  describe(p, m, n);
+  describe(p, m, n, true);
   p.s = scalars(tau, kappa, rng, reg_coeff, 0.0f);
   return reg_coeff != 0.0f ? launch<BwdOp<true, kGPT>>(d, p, s)
                            : launch<BwdOp<false, kGPT>>(d, p, s);
@@ -1076,7 +1114,7 @@ cudaError_t stream_backward(const Device& d, const StreamMatrix* m, int n, float
 
 cudaError_t stream_hard_compress(const Device& d, const StreamMatrix* m, int n, cudaStream_t s) {
   StreamParams p;
-  describe(p, m, n);
+  describe(p, m, n, true);
   p.s = scalars(1.0f, 0.0f, {0, 0, 0}, 0.0f, 0.0f);
   return launch<CompressOp<kGPT>>(d, p, s);
 }
@@ -1084,7 +1122,7 @@ cudaError_t stream_hard_compress(const Device& d, const StreamMatrix* m, int n, 
 cudaError_t stream_mask_stats(const Device& d, const StreamMatrix* m, int n, float tau, float kappa,
                               RngArgs rng, cudaStream_t s) {
   StreamParams p;
-  describe(p, m, n);
+  describe(p, m, n, false);
   p.s = scalars(tau, kappa, rng, 0.0f, 0.0f);
   return launch<StatsOp<kGPT>>(d, p, s);
 }
@@ -1092,7 +1130,7 @@ cudaError_t stream_mask_stats(const Device& d, const StreamMatrix* m, int n, flo
 cudaError_t stream_forward_stats(const Device& d, const StreamMatrix* m, int n, float tau,
                                  float kappa, RngArgs rng, cudaStream_t s) {
   StreamParams p;
-  describe(p, m, n);
+  describe(p, m, n, false);
   p.s = scalars(tau, kappa, rng, 0.0f, 0.0f);
   return launch<FwdStatsOp<kGPT>>(d, p, s);
 }
