@@ -411,7 +411,8 @@ def run_gpu(args):
 
 def run_extras(blk, peak, dev, reps=20, spmm_tile_n=0):
     """The entry points beyond the step, on the same resident block: logits
-    from a given mask (6.125 B/weight: codes in, logits out), the convergence
+    from a given mask (6.125 B/weight: codes in, logits out; one batched
+    launch), the convergence
     diagnostics (6.5 B/weight: logits and previous draws in, draws out) and
     the forward with the diagnostics in the same pass (10.5 B/weight), each
     over all matrices (one launch per matrix), CUDA-event timed."""
@@ -425,11 +426,13 @@ def run_extras(blk, peak, dev, reps=20, spmm_tile_n=0):
     l1 = [torch.empty((m["x"].rows,), dtype=torch.int32, device=dev) for m in blk.mats]
     mp = [torch.empty((m["x"].rows,), dtype=torch.float32, device=dev) for m in blk.mats]
 
+    # logits from the step's compressed masks: one batched launch per block
+    pfm_arr = mk.matrix_array([{"meta": m["meta_out"], "logits_out": m["logits_out"]}
+                               for m in blk.mats])
+
     def prior_from_mask():
-        for m in blk.mats:
-            st = L.maskllm_prior_from_mask(m["meta_out"].data_ptr(), m["x"].rows, m["x"].cols,
-                                           1.0, 0.0, m["logits_out"].data_ptr(), s)
-            assert st == 0
+        st = L.maskllm_prior_from_mask_batched(pfm_arr, len(blk.mats), 1.0, 0.0, s)
+        assert st == 0
 
     def mask_stats(step):
         for i, m in enumerate(blk.mats):
@@ -469,7 +472,7 @@ def run_extras(blk, peak, dev, reps=20, spmm_tile_n=0):
         gbs = bpw * blk.weights / sec / 1e9
         out[name] = {"us_per_block": round(sec * 1e6, 2), "GB_per_s": round(gbs, 1),
                      "frac_of_hbm": round(gbs / peak, 4), "bytes_per_weight": bpw,
-                     "launches_per_block": len(blk.mats)}
+                     "launches_per_block": 1 if name == "prior_from_mask" else len(blk.mats)}
     out["perm_search"] = run_perm_search(blk, dev)
     blk.mk.maskllm_test_spmm_tile_n(spmm_tile_n)
     try:

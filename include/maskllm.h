@@ -368,7 +368,7 @@ maskllm_status maskllm_forward_stats(const uint16_t* W, const float* logits,
 #define MASKLLM_MAX_BATCH 16
 
 typedef struct {
-  const uint16_t* W;          /* bf16 [rows, cols] (all operations) */
+  const uint16_t* W;          /* bf16 [rows, cols] (all operations but prior_from_mask) */
   const float* logits;        /* fp32 [rows, cols/4, 6] (forward, backward, compress) */
   const uint16_t* grad_W_out; /* bf16 [rows, cols] (backward) */
   int64_t rows;
@@ -382,6 +382,8 @@ typedef struct {
   uint16_t* values_out;       /* hard_compress output */
   uint32_t* meta_out;         /* hard_compress output */
   uint8_t* idx_out;           /* hard_compress output, nullable */
+  const uint32_t* meta;       /* prior_from_mask input: 4-bit codes u32 [rows, cols/32]
+                                 (logits_out is its output; W is not read) */
 } maskllm_matrix;
 
 /* n >= 1 matrices; the noise of matrix i uses (seed, step, mats[i].tensor_id). */
@@ -395,6 +397,10 @@ maskllm_status maskllm_backward_batched(const maskllm_matrix* mats, int32_t n, f
                                         float reg_coeff, maskllm_stream_t stream);
 maskllm_status maskllm_hard_compress_batched(const maskllm_matrix* mats, int32_t n,
                                              maskllm_stream_t stream);
+/* maskllm_prior_from_mask over a batch (MaskLLM Table 2): reads meta, writes
+ * logits_out of every matrix; high and low as in the single call. */
+maskllm_status maskllm_prior_from_mask_batched(const maskllm_matrix* mats, int32_t n, float high,
+                                               float low, maskllm_stream_t stream);
 
 /* ---- Failure detection -------------------------------------------------
  * The pipelined kernels wait on shared-memory barriers for their bulk copies.

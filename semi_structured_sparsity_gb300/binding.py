@@ -25,7 +25,8 @@ STATUS = {0: "MASKLLM_OK", 1: "MASKLLM_ERR_INVALID_ARG", 2: "MASKLLM_ERR_SHAPE",
 EXPORTS = ("maskllm_prior_init", "maskllm_forward", "maskllm_backward",
            "maskllm_hard_compress", "maskllm_decompress", "maskllm_noise_words",
            "maskllm_prior_init_batched", "maskllm_forward_batched", "maskllm_backward_batched",
-           "maskllm_hard_compress_batched", "maskllm_prior_from_mask", "maskllm_mask_stats",
+           "maskllm_hard_compress_batched", "maskllm_prior_from_mask",
+           "maskllm_prior_from_mask_batched", "maskllm_mask_stats",
            "maskllm_perm_shift", "maskllm_perm_metric", "maskllm_permute_columns",
            "maskllm_perm_swap_gains", "maskllm_perm_search", "maskllm_perm_search_static",
            "maskllm_spmm", "maskllm_forward_stats",
@@ -48,7 +49,8 @@ class maskllm_matrix(C.Structure):
                 ("rows", C.c_int64), ("cols", C.c_int64), ("tensor_id", C.c_uint32),
                 ("logits_out", C.c_void_p), ("W_out", C.c_void_p), ("row_sq_out", C.c_void_p),
                 ("probs_out", C.c_void_p), ("dlogits_out", C.c_void_p),
-                ("values_out", C.c_void_p), ("meta_out", C.c_void_p), ("idx_out", C.c_void_p)]
+                ("values_out", C.c_void_p), ("meta_out", C.c_void_p), ("idx_out", C.c_void_p),
+                ("meta", C.c_void_p)]
 
 
 class MaskLLMError(RuntimeError):
@@ -84,6 +86,7 @@ def lib() -> C.CDLL:
         L.maskllm_backward_batched.argtypes = [mp, i32, f32, f32, u64, u32, f32, vp]
         L.maskllm_hard_compress_batched.argtypes = [mp, i32, vp]
         L.maskllm_prior_from_mask.argtypes = [vp, i64, i64, f32, f32, vp, vp]
+        L.maskllm_prior_from_mask_batched.argtypes = [mp, i32, f32, f32, vp]
         L.maskllm_mask_stats.argtypes = [vp, vp, i64, i64, f32, f32, maskllm_rng, vp, vp, vp, vp]
         L.maskllm_set_wait_timeout.argtypes = [u64]
         L.maskllm_test_withhold_loads.argtypes = [i32]
@@ -239,22 +242,30 @@ def maskllm_status_string(status: int) -> str:
 # ---------------------------------------------------------------------------
 # Batched calls.  `mats` is a list of dicts with tensor entries named like the
 # fields of maskllm_matrix (W, logits, grad_W_out, logits_out, W_out,
-# row_sq_out, probs_out, dlogits_out, values_out, meta_out, idx_out) and an
-# optional int tensor_id.
+# row_sq_out, probs_out, dlogits_out, values_out, meta_out, idx_out, meta) and
+# an optional int tensor_id.  The shape comes from W (bf16 [rows, cols]), or
+# from meta (int32 [rows, cols/32]) when there is no W.
 # ---------------------------------------------------------------------------
 
 _TENSOR_FIELDS = ("W", "logits", "grad_W_out", "logits_out", "W_out", "row_sq_out",
-                  "probs_out", "dlogits_out", "values_out", "meta_out", "idx_out")
+                  "probs_out", "dlogits_out", "values_out", "meta_out", "idx_out", "meta")
 
 
 def matrix_array(mats):
     arr = (maskllm_matrix * len(mats))()
     for a, m in zip(arr, mats):
-        W = m["W"]
-        if not (isinstance(W, torch.Tensor) and W.is_cuda and W.dtype == torch.bfloat16
-                and W.dim() == 2 and W.is_contiguous()):
-            raise ValueError("W must be a contiguous 2-D bf16 CUDA tensor")
-        a.rows, a.cols = W.shape
+        W = m.get("W")
+        if W is None and m.get("meta") is not None:
+            meta = m["meta"]
+            if not (isinstance(meta, torch.Tensor) and meta.dtype == torch.int32
+                    and meta.dim() == 2):
+                raise ValueError("meta must be a 2-D int32 CUDA tensor")
+            a.rows, a.cols = meta.shape[0], 32 * meta.shape[1]
+        else:
+            if not (isinstance(W, torch.Tensor) and W.is_cuda and W.dtype == torch.bfloat16
+                    and W.dim() == 2 and W.is_contiguous()):
+                raise ValueError("W must be a contiguous 2-D bf16 CUDA tensor")
+            a.rows, a.cols = W.shape
         a.tensor_id = int(m.get("tensor_id", 0))
         for f in _TENSOR_FIELDS:
             t = m.get(f)
@@ -287,6 +298,12 @@ def maskllm_hard_compress_batched(mats, stream=None):
     arr = matrix_array(mats)
     _check("maskllm_hard_compress_batched",
            lib().maskllm_hard_compress_batched(arr, len(mats), _stream(stream)))
+
+
+def maskllm_prior_from_mask_batched(mats, high, low, stream=None):
+    arr = matrix_array(mats)
+    _check("maskllm_prior_from_mask_batched", lib().maskllm_prior_from_mask_batched(
+        arr, len(mats), high, low, _stream(stream)))
 
 
 def maskllm_set_wait_timeout(nanoseconds: int) -> None:

@@ -59,9 +59,10 @@ cudaError_t stream_mask_stats(const Device& d, const StreamMatrix* m, int n, flo
 // out3 = L1 per row, out4 = max-probability sum per row (all nullable).
 cudaError_t stream_forward_stats(const Device& d, const StreamMatrix* m, int n, float tau,
                                  float kappa, RngArgs rng, cudaStream_t s);
-cudaError_t launch_prior_from_mask(const Device& d, const uint32_t* meta, int64_t rows,
-                                   int64_t cols, float high, float low, float* logits,
-                                   cudaStream_t s);
+// Logits from 2:4 codes, up to kMaxBatch matrices in one launch
+// (kernels_pack.cu): W = the codes (u32 [rows, cols/32]), out0 = logits.
+cudaError_t launch_prior_from_mask(const Device& d, const StreamMatrix* m, int n, float high,
+                                   float low, cudaStream_t s);
 // ---- channel permutation before pruning (kernels_perm.cu) -----------------
 
 constexpr int32_t kPermBadPermutation = -1;   // search / gains outcome codes

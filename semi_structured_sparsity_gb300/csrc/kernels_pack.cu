@@ -51,36 +51,53 @@ __global__ void __launch_bounds__(256) decompress_kernel(const uint4* __restrict
 constexpr uint64_t kCandOfCode = 0xF542FF31FFF0FFFFull;
 constexpr int kPfmThreads = 256;
 
-// A warp covers 64 groups (32 threads x 2): each thread reads the metadata
-// byte of its two groups, writes its 48 bytes of logits into a warp-private
-// shared buffer, and the warp then stores the buffer with 16-byte stores that
-// are contiguous across lanes.
-__global__ void __launch_bounds__(kPfmThreads) prior_from_mask_kernel(
-    const uint8_t* __restrict__ meta_bytes, float4* __restrict__ L, int64_t items, float high,
-    float low) {
+// A batch of matrices as one list of warp tiles: a tile is 32 code bytes
+// (64 groups) of one matrix; matrix m owns tiles [tile_begin[m],
+// tile_begin[m + 1]).
+struct PfmBatch {
+  const uint8_t* meta[kMaxBatch];   // code bytes: group k at nibble k % 2 of byte k / 2
+  float4* L[kMaxBatch];             // logits, 6 floats per group
+  int64_t items[kMaxBatch];         // code bytes (pairs of groups) of the matrix
+  int64_t tile_begin[kMaxBatch + 1];
+  int32_t n;
+  float high, low;
+};
+
+// Each warp takes tiles in a grid-stride loop (ascending, so the matrix of
+// the next tile is found by moving forward through tile_begin): each thread
+// reads the code byte of its two groups, writes its 48 bytes of logits into
+// a warp-private shared buffer, and the warp stores the buffer with 16-byte
+// stores that are contiguous across lanes.
+__global__ void __launch_bounds__(kPfmThreads) prior_from_mask_kernel(const __grid_constant__
+                                                                      PfmBatch p) {
   __shared__ __align__(16) float4 buf[kPfmThreads / 32][96];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (kPfmThreads / 32);
-  for (int64_t tile = blockIdx.x * (int64_t)(kPfmThreads / 32) + warp; tile * 32 < items;
+  const int64_t tiles = p.tile_begin[p.n];
+  int m = 0;
+  for (int64_t tile = blockIdx.x * (int64_t)(kPfmThreads / 32) + warp; tile < tiles;
        tile += warps_total) {
-    const int64_t item = tile * 32 + lane;          // two groups: 2*item, 2*item + 1
-    const int64_t left = items - tile * 32;         // items in this tile (<= 32 used)
+    while (tile >= p.tile_begin[m + 1]) ++m;
+    const int64_t local = tile - p.tile_begin[m];
+    const int64_t item = local * 32 + lane;          // two groups: 2*item, 2*item + 1
+    const int64_t left = p.items[m] - local * 32;    // items in this tile (<= 32 used)
     const int n_items = static_cast<int>(left < 32 ? left : 32);
     if (lane < n_items) {
-      const uint32_t b = __ldcs(meta_bytes + item);
+      const uint32_t b = __ldcs(p.meta[m] + item);
       float v[12];
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
-        const uint32_t cand = static_cast<uint32_t>(kCandOfCode >> (4 * ((b >> (4 * g)) & 0xFu))) & 0xFu;
+        const uint32_t cand =
+            static_cast<uint32_t>(kCandOfCode >> (4 * ((b >> (4 * g)) & 0xFu))) & 0xFu;
 #pragma unroll
-        for (int c = 0; c < kCand; ++c) v[6 * g + c] = (static_cast<uint32_t>(c) == cand) ? high : low;
+        for (int c = 0; c < kCand; ++c) v[6 * g + c] = (static_cast<uint32_t>(c) == cand) ? p.high : p.low;
       }
       buf[warp][3 * lane + 0] = make_float4(v[0], v[1], v[2], v[3]);
       buf[warp][3 * lane + 1] = make_float4(v[4], v[5], v[6], v[7]);
       buf[warp][3 * lane + 2] = make_float4(v[8], v[9], v[10], v[11]);
     }
     __syncwarp();
-    float4* dst = L + 3 * tile * 32;
+    float4* dst = p.L[m] + 3 * local * 32;
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
       const int q = lane + 32 * k;                    // 16-byte chunk of the tile
@@ -122,15 +139,23 @@ cudaError_t launch_decompress(const Device& d, const uint16_t* values, const uin
   return cudaGetLastError();
 }
 
-cudaError_t launch_prior_from_mask(const Device& d, const uint32_t* meta, int64_t rows,
-                                   int64_t cols, float high, float low, float* logits,
-                                   cudaStream_t s) {
-  const int64_t items = rows * cols / 8;   // pairs of groups = metadata bytes
-  const int64_t tiles = (items + 31) / 32;
-  const int64_t want = (tiles + kPfmThreads / 32 - 1) / (kPfmThreads / 32);
+cudaError_t launch_prior_from_mask(const Device& d, const StreamMatrix* mats, int n, float high,
+                                   float low, cudaStream_t s) {
+  if (n < 1 || n > kMaxBatch) return cudaErrorInvalidValue;
+  PfmBatch p;
+  p.n = n;
+  p.high = high;
+  p.low = low;
+  p.tile_begin[0] = 0;
+  for (int i = 0; i < n; ++i) {
+    p.meta[i] = static_cast<const uint8_t*>(mats[i].W);
+    p.L[i] = static_cast<float4*>(mats[i].out0);
+    p.items[i] = mats[i].rows * mats[i].cols / 8;   // code bytes = pairs of groups
+    p.tile_begin[i + 1] = p.tile_begin[i] + (p.items[i] + 31) / 32;
+  }
+  const int64_t want = (p.tile_begin[n] + kPfmThreads / 32 - 1) / (kPfmThreads / 32);
   const int64_t cap = 8LL * d.num_sms;
-  prior_from_mask_kernel<<<static_cast<int>(want < cap ? want : cap), kPfmThreads, 0, s>>>(
-      reinterpret_cast<const uint8_t*>(meta), reinterpret_cast<float4*>(logits), items, high, low);
+  prior_from_mask_kernel<<<static_cast<int>(want < cap ? want : cap), kPfmThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -149,13 +149,23 @@ maskllm_status check_compress(const maskllm_matrix& m, Spans& sp) {
   return MASKLLM_OK;
 }
 
+maskllm_status check_prior_from_mask(const maskllm_matrix& m, Spans& sp) {
+  const void* ptrs[] = {m.meta, m.logits_out};
+  MK_TRY(check_ptrs(ptrs, 2));
+  MK_TRY(check_shape(m.rows, m.cols));
+  const uint64_t n = weights(m);
+  sp.input(m.meta, n / 8);
+  sp.output(m.logits_out, 6 * n);
+  return MASKLLM_OK;
+}
+
 maskllm_status finish(cudaError_t e) { return e == cudaSuccess ? MASKLLM_OK : cuda_fail(e); }
 
-enum class Op { kPrior, kForward, kBackward, kCompress };
+enum class Op { kPrior, kForward, kBackward, kCompress, kPriorFromMask };
 
 struct Call {
   Op op;
-  float tau = 1.0f, kappa = 0.0f, reg = 0.0f, scale = 1.0f;
+  float tau = 1.0f, kappa = 0.0f, reg = 0.0f, scale = 1.0f, high = 0.0f, low = 0.0f;
   uint64_t seed = 0;
   uint32_t step = 0;
 };
@@ -181,48 +191,49 @@ StreamMatrix to_stream(const maskllm_matrix& m, Op op) {
       s.out1 = m.meta_out;
       s.out2 = m.idx_out;
       break;
+    case Op::kPriorFromMask:
+      s.W = m.meta;
+      s.L = nullptr;
+      s.G = nullptr;
+      s.out0 = m.logits_out;
+      break;
   }
   return s;
+}
+
+// The validation of one matrix for the call's operation (appends its spans).
+maskllm_status check_matrix(Op op, const maskllm_matrix& m, Spans& sp) {
+  switch (op) {
+    case Op::kPrior: return check_prior(m, sp);
+    case Op::kForward: return check_forward(m, sp);
+    case Op::kBackward: return check_backward(m, sp);
+    case Op::kCompress: return check_compress(m, sp);
+    case Op::kPriorFromMask: return check_prior_from_mask(m, sp);
+  }
+  return MASKLLM_ERR_INVALID_ARG;
 }
 
 maskllm_status run(const Call& c, const maskllm_matrix* mats, int32_t n, cudaStream_t s) {
   if (mats == nullptr || n < 1) return MASKLLM_ERR_INVALID_ARG;
   if (c.op == Op::kForward || c.op == Op::kBackward) MK_TRY(check_temperature(c.tau, c.kappa));
-  if (!isfinite(c.reg) || !isfinite(c.scale)) return MASKLLM_ERR_INVALID_ARG;
+  if (!isfinite(c.reg) || !isfinite(c.scale) || !isfinite(c.high) || !isfinite(c.low))
+    return MASKLLM_ERR_INVALID_ARG;
   // validate everything before launching anything
   for (int32_t b = 0; b < n; b += kMaxBatch) {
     const int32_t nb = n - b < kMaxBatch ? n - b : kMaxBatch;
     Spans sp;
-    for (int32_t i = 0; i < nb; ++i) {
-      const maskllm_matrix& m = mats[b + i];
-      switch (c.op) {
-        case Op::kPrior: MK_TRY(check_prior(m, sp)); break;
-        case Op::kForward: MK_TRY(check_forward(m, sp)); break;
-        case Op::kBackward: MK_TRY(check_backward(m, sp)); break;
-        case Op::kCompress: MK_TRY(check_compress(m, sp)); break;
-      }
-    }
+    for (int32_t i = 0; i < nb; ++i) MK_TRY(check_matrix(c.op, mats[b + i], sp));
     MK_TRY(sp.check());
   }
   if (n > kMaxBatch) {
     // outputs of one launch must not overlap inputs or outputs of another
     for (int32_t i = 0; i < n; ++i) {
       Spans one;
-      switch (c.op) {
-        case Op::kPrior: check_prior(mats[i], one); break;
-        case Op::kForward: check_forward(mats[i], one); break;
-        case Op::kBackward: check_backward(mats[i], one); break;
-        case Op::kCompress: check_compress(mats[i], one); break;
-      }
+      check_matrix(c.op, mats[i], one);
       for (int32_t j = 0; j < n; ++j) {
         if (j == i) continue;
         Spans other;
-        switch (c.op) {
-          case Op::kPrior: check_prior(mats[j], other); break;
-          case Op::kForward: check_forward(mats[j], other); break;
-          case Op::kBackward: check_backward(mats[j], other); break;
-          case Op::kCompress: check_compress(mats[j], other); break;
-        }
+        check_matrix(c.op, mats[j], other);
         for (int o = 0; o < one.n_out; ++o) {
           for (int k = 0; k < other.n_in; ++k)
             if (overlaps(one.out[o], other.in[k])) return MASKLLM_ERR_ALIAS;
@@ -249,6 +260,7 @@ maskllm_status run(const Call& c, const maskllm_matrix* mats, int32_t n, cudaStr
       case Op::kForward: e = stream_forward(d, sm, nb, c.tau, c.kappa, rng, probs, s); break;
       case Op::kBackward: e = stream_backward(d, sm, nb, c.tau, c.kappa, rng, c.reg, s); break;
       case Op::kCompress: e = stream_hard_compress(d, sm, nb, s); break;
+      case Op::kPriorFromMask: e = launch_prior_from_mask(d, sm, nb, c.high, c.low, s); break;
     }
     if (e != cudaSuccess) return cuda_fail(e);
   }
@@ -416,20 +428,23 @@ maskllm_status maskllm_noise_words(maskllm_rng rng, int64_t group_begin, int64_t
 maskllm_status maskllm_prior_from_mask(const uint32_t* meta, int64_t rows, int64_t cols,
                                        float high, float low, float* logits_out,
                                        maskllm_stream_t stream) {
-  const void* ptrs[] = {meta, logits_out};
-  MK_TRY(maskllm::check_ptrs(ptrs, 2));
-  MK_TRY(maskllm::check_shape(rows, cols));
-  if (!isfinite(high) || !isfinite(low)) return MASKLLM_ERR_INVALID_ARG;
-  const uint64_t n = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols);
-  maskllm::Spans sp;
-  sp.input(meta, n / 8);
-  sp.output(logits_out, 6 * n);
-  MK_TRY(sp.check());
-  maskllm::Device d;
-  cudaError_t e = maskllm::current_device(&d);
-  if (e != cudaSuccess) return maskllm::cuda_fail(e);
-  return maskllm::finish(
-      maskllm::launch_prior_from_mask(d, meta, rows, cols, high, low, logits_out, stream));
+  maskllm_matrix m{};
+  m.meta = meta;
+  m.rows = rows;
+  m.cols = cols;
+  m.logits_out = logits_out;
+  Call c{Op::kPriorFromMask};
+  c.high = high;
+  c.low = low;
+  return maskllm::run(c, &m, 1, stream);
+}
+
+maskllm_status maskllm_prior_from_mask_batched(const maskllm_matrix* mats, int32_t n, float high,
+                                               float low, maskllm_stream_t stream) {
+  Call c{Op::kPriorFromMask};
+  c.high = high;
+  c.low = low;
+  return maskllm::run(c, mats, n, stream);
 }
 
 maskllm_status maskllm_mask_stats(const float* logits, const uint8_t* prev_idx, int64_t rows,

@@ -148,6 +148,24 @@ def test_batched_alias_across_launches(L):
     assert L.maskllm_prior_init_batched(arr, n, 1.0, None) == ALIAS
 
 
+def test_prior_from_mask_batched_validation(L):
+    from semi_structured_sparsity_gb300 import binding
+    arr = (binding.maskllm_matrix * 2)()
+    arr[0] = _mat(logits_out=B)
+    arr[0].meta = A
+    arr[1] = _mat(logits_out=D)               # no codes
+    assert L.maskllm_prior_from_mask_batched(arr, 2, 1.0, 0.0, None) == INVALID
+    arr[1].meta = E
+    assert L.maskllm_prior_from_mask_batched(arr, 2, float("nan"), 0.0, None) == INVALID
+    arr[1].logits_out = A + 16                # writes over matrix 0's codes
+    assert L.maskllm_prior_from_mask_batched(arr, 2, 1.0, 0.0, None) == ALIAS
+    arr[1].logits_out = D + 4                 # misaligned output
+    assert L.maskllm_prior_from_mask_batched(arr, 2, 1.0, 0.0, None) == ALIGN
+    arr[1] = _mat(logits_out=D, rows=4, cols=40)
+    arr[1].meta = E
+    assert L.maskllm_prior_from_mask_batched(arr, 2, 1.0, 0.0, None) == SHAPE
+
+
 def test_next_entry_points_validation(L):
     r = _rng()
     assert L.maskllm_prior_from_mask(A, 4, 64, float("inf"), 0.0, B, None) == INVALID

@@ -34,6 +34,34 @@ def test_prior_from_mask_bit_exact(rows, cols):
     assert_bits_equal(bits32(L), want.view(np.uint32), "logits from mask")
 
 
+def _random_codes(rows, cols, seed):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    return torch.randint(-2**31, 2**31 - 1, (rows, cols // 32), generator=gen, device="cuda",
+                         dtype=torch.int64).to(torch.int32)   # every code, valid or not
+
+
+@pytest.mark.parametrize("n", [len(SHAPES), 20])
+def test_prior_from_mask_batched_matches_single_calls_and_oracle(n):
+    """One batched launch over matrices whose last chunks are full (codes
+    copied into the stage) and ragged (codes loaded per thread); 20 matrices
+    take two launches."""
+    shapes = [SHAPES[i % len(SHAPES)] for i in range(n)]
+    mats = []
+    for i, (rows, cols) in enumerate(shapes):
+        meta = _random_codes(rows, cols, 900 + i)
+        mats.append({"meta": meta, "logits_out": torch.full((rows, cols // 4, 6), float("nan"),
+                                                            device="cuda")})
+    mk.maskllm_prior_from_mask_batched(mats, 2.5, -1.0)
+    torch.cuda.synchronize()
+    for (rows, cols), m in zip(shapes, mats):
+        single = mk.maskllm_prior_from_mask(m["meta"], rows, cols, 2.5, -1.0)
+        torch.cuda.synchronize()
+        assert torch.equal(single.view(torch.int32), m["logits_out"].view(torch.int32))
+        want = orc.prior_from_mask(bits32(m["meta"]), rows, cols, 2.5, -1.0)
+        assert_bits_equal(bits32(m["logits_out"]), want.view(np.uint32), "batched logits")
+
+
 def test_prior_from_mask_round_trips_hard_compress():
     W, L, _ = wl.random_case(64, 4096, seed=77, device="cuda")
     vals, meta, idx = mk.maskllm_hard_compress(W, L, want_idx=True)
