@@ -214,13 +214,24 @@ def traffic_table():
 STREAM_SOURCES = ("device_common.cuh", "kernels_stream.cu", "pipeline.cuh")
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed
+    (string literals in these sources hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_digest() -> str:
+    """Digest of the code compiled into the stream kernels (comments and
+    whitespace excluded: they change no instruction)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "semi_structured_sparsity_gb300", "csrc")
     for fn in STREAM_SOURCES:
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, fn)) as f:
+            h.update(fn.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:12]
 
 

@@ -339,12 +339,13 @@ maskllm_status maskllm_perm_search_static(const uint16_t* W, int64_t rows, int64
                                           int32_t* shift_out, maskllm_stream_t stream);
 
 /* The forward and the convergence diagnostics of one step in a single pass
- * (MaskLLM Fig. 5; the optional outputs of maskllm_forward): W_out and
- * row_sq_out exactly as maskllm_forward computes them (bit-identical), and
- * idx_out, l1_row_out, maxprob_row_out exactly as maskllm_mask_stats
- * computes them for the same step.  The noisy logits z the forward forms
- * give the draws, so the diagnostics cost a few instructions per group and
- * 2 bytes of traffic per group instead of a second pass over the logits.
+ * (MaskLLM Fig. 5; the optional outputs of maskllm_forward): W_out, idx_out
+ * and l1_row_out are bit-identical to those of maskllm_forward and
+ * maskllm_mask_stats for the same step; row_sq_out and maxprob_row_out are
+ * the same row sums added in another order (they agree to about 1e-6
+ * relative).  The noisy logits z the forward forms give the draws, so the
+ * diagnostics cost no second pass over the logits: 0.5 bytes of traffic per
+ * group more than the forward (the draws out, the previous draws in).
  *   W, logits, W_out, row_sq_out   as maskllm_forward (row_sq_out nullable)
  *   prev_idx, idx_out, l1_row_out, maxprob_row_out   as maskllm_mask_stats
  *                                  (all nullable; l1_row_out needs prev_idx)

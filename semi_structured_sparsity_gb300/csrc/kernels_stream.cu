@@ -659,9 +659,11 @@ struct StatsOp : OpBase<GPT, 4> {
 // optional outputs of the "MaskLLM" Fig. 5 quantities): the noisy logits z
 // the forward forms anyway give the draw (their first maximum), and the
 // scaled logits fl32(kappa * L) it forms on the way give the distribution's
-// largest probability.  W' and row_sq are computed exactly as in FwdOp; the
-// draws, L1 and max-probability exactly as in StatsOp.  Row quantities: 0
-// row_sq, 1 L1 distance, 2 max-probability sum.
+// largest probability.  W' is computed exactly as in FwdOp, the draws and
+// the L1 distances exactly as in StatsOp; the row sums of squares and of
+// the maximum probabilities are the same sums added in this op's own order
+// (per-thread partials, in the thread's consumed W slot).  Row quantities:
+// 0 row_sq, 1 L1 distance, 2 max-probability sum.
 template <int GPT>
 struct FwdStatsOp : OpBase<GPT, 4> {
   static constexpr bool kTable = true, kStaged = false, kWarpWide = false;
