@@ -28,3 +28,25 @@ def test_sharded_pass_runs_and_shards_reproduce_the_whole():
     parts = [orc.forward(Wb[a:b], L[a:b], wl.tau, wl.kappa, 0, 0, tid, row_begin=a)[0]
              for a, b in ((0, 2), (2, 5), (5, 6))]
     assert np.array_equal(np.concatenate(parts), whole)
+
+
+def test_source_digest_follows_code_not_comments():
+    """A stored DRAM-traffic figure stays valid while only comments or
+    whitespace of the stream-kernel sources change, and no longer once the
+    code does."""
+    a = "int f(int x) {  // the count\n  return x + 1; /* one\n more */ }\n"
+    b = "int f(int x) {\n\n  return x + 1;   }  // comments differ\n"
+    c = "int f(int x) { return x + 2; }\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert len(bench.kernel_source_digest()) == 12
+
+
+def test_traffic_table_reads_the_committed_summary():
+    tt = bench.traffic_table()
+    for k in bench.KERNELS:
+        bytes_, digest = tt[(k, "llama2_7b_block")]
+        # DRAM bytes of one launch within 5% of the algorithmic bytes
+        alg = bench.BYTES_PER_WEIGHT[k] * W.WORKLOADS["llama2_7b_block"].weights
+        assert 0.95 * alg <= bytes_ <= 1.01 * alg
+        assert len(digest) == 12
