@@ -109,6 +109,7 @@ struct Chunk {
   int64_t g0;       // first group, matrix-local
   int64_t row0;     // first row
   int32_t nrows;    // whole rows ending in this chunk (0 when a long row continues)
+  int32_t obuf;     // staged outputs: which of the stage's output buffers
 };
 
 __device__ __forceinline__ int64_t units_of(const MatDesc& d) {
@@ -307,6 +308,10 @@ struct OpBase {
   static constexpr bool kPartialsInCopyTarget = false;
   // chunk the matrices flat (no per-row sums: prior, backward, compress)
   static constexpr bool kFlat = false;
+  // staged outputs: buffers per stage (chunk n of a stage's ring writes
+  // buffer (n / kStages) % kOutBuffers), kOutBufBytes apart
+  static constexpr int kOutBuffers = 1;
+  static constexpr uint32_t kOutBufBytes = 0;
 };
 
 template <int GPT>
@@ -314,8 +319,13 @@ struct PriorOp : OpBase<GPT, 4> {
   static constexpr bool kFlat = true;
   static constexpr bool kTable = false, kStaged = true, kWarpWide = false;
   static constexpr bool kOutOverlapsInput = false;   // W in, logits out: separate regions
-  static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
+  // two output buffers per stage: the consumers write one while the bulk
+  // store of the stage's previous chunk still reads the other (there is no
+  // Gumbel table, so the shared memory holds them)
+  static constexpr int kOutBuffers = 2;
+  static constexpr uint32_t kOutBufBytes = kChunkGroups * 24;
   static constexpr uint32_t kOutOffset = kChunkGroups * 8;
+  static constexpr uint32_t kStageBytes = kOutOffset + kOutBuffers * kOutBufBytes;
   static constexpr uint32_t kOutBytesPerGroup = 24;
 
   __device__ static void issue(const MatDesc& d, const Chunk& c, uint8_t* st, uint64_t* bar) {
@@ -324,8 +334,8 @@ struct PriorOp : OpBase<GPT, 4> {
     bulk_load(st, static_cast<const uint8_t*>(d.W) + c.g0 * 8, wb, bar);
   }
 
-  __device__ static void consume(const StreamParams& p, const MatDesc&, const Chunk&, uint8_t* st,
-                                 int t, const float*, float*) {
+  __device__ static void consume(const StreamParams& p, const MatDesc&, const Chunk& c,
+                                 uint8_t* st, int t, const float*, float*) {
     uint32_t w[2 * GPT];
     load_w<GPT>(st, t, w);
     float out[6 * GPT];
@@ -342,7 +352,7 @@ struct PriorOp : OpBase<GPT, 4> {
       o[4] = __fmul_rn(s, __fadd_rn(a1, a3));
       o[5] = __fmul_rn(s, __fadd_rn(a2, a3));
     }
-    store_l<GPT>(st + kOutOffset, t, out);
+    store_l<GPT>(st + kOutOffset + c.obuf * kOutBufBytes, t, out);
   }
 };
 
@@ -814,7 +824,8 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
     }
     if (Op::kStaged && lane == 0) {
       bulk_store(static_cast<uint8_t*>(d.out0) + c.g0 * Op::kOutBytesPerGroup,
-                 st + Op::kOutOffset, static_cast<uint32_t>(c.ng) * Op::kOutBytesPerGroup);
+                 st + Op::kOutOffset + c.obuf * Op::kOutBufBytes,
+                 static_cast<uint32_t>(c.ng) * Op::kOutBytesPerGroup);
       bulk_commit();
     }
   };
@@ -845,6 +856,7 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
       }
     }
     if (lane == 0) {
+      c.obuf = static_cast<int32_t>((n / S) % Op::kOutBuffers);
       held[s] = c;
       // a staged store may still be reading this stage's output region:
       // wait before the refill if the copies land there, after it if not
@@ -860,7 +872,11 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
       __syncwarp();
     }
     if (lane == 0) {
-      if (Op::kStaged && !Op::kOutOverlapsInput) bulk_wait_reads();
+      // the store that last read the output buffer this chunk will write --
+      // the stage's chunk kOutBuffers turns ago -- has at most
+      // S (kOutBuffers - 1) stores committed after it
+      if (Op::kStaged && !Op::kOutOverlapsInput)
+        bulk_wait_reads_but<S * (Op::kOutBuffers - 1)>();
       mbar_arrive(&full[s]);   // with the copies' bytes, completes the phase
     }
     __syncwarp();

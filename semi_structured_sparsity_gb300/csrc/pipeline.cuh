@@ -111,6 +111,13 @@ __device__ __forceinline__ void bulk_wait_reads() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Wait until at most N of the most recently committed bulk stores may still
+// be reading shared memory (every older one has finished reading).
+template <int N>
+__device__ __forceinline__ void bulk_wait_reads_but() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 // Wait until every committed bulk store has completed.
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
