@@ -24,8 +24,11 @@
 //   warp 1     allocates the pair's tensor memory (both CTAs together); in
 //              rank 0 one thread waits for each stage, copies the stage's
 //              metadata into tensor memory (tcgen05.cp, performed in order
-//              with its MMAs), issues the four MMAs and commits them to the
-//              stage's "empty" barrier in both CTAs, the last to "done".
+//              before its later MMAs; two sets of metadata columns, and
+//              before reusing a set it waits for the commit of the MMAs
+//              that read it two stages earlier), issues the four MMAs and
+//              commits them to the stage's "empty" barrier in both CTAs,
+//              the last to "done".
 //   warp 2     (rank 1) forwards "this CTA's copies landed" to rank 0.
 //   warps 4-7  one tensor-memory lane per thread.  Per stage they write the
 //              stage's metadata into shared memory in the order the sparse
@@ -323,6 +326,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int kt = 0; kt < nk; ++kt) {
         const int s = kt % kStages;
         if (!mbar_wait_bounded(&full[s], (kt / kStages) & 1, wait_ns, abort_flag)) {
+          raise(abort_flag, peer);
+          break;
+        }
+        // The copy below overwrites the metadata columns that the MMAs of
+        // stage kt - 2 read, and a tcgen05.cp is not ordered after earlier
+        // MMAs of the same thread: wait for their commit (that stage's
+        // "empty" phase), normally complete long before.
+        if (kt >= 2 && !mbar_wait_bounded(&empty[(kt - 2) % kStages], ((kt - 2) / kStages) & 1,
+                                          wait_ns, abort_flag)) {
           raise(abort_flag, peer);
           break;
         }
