@@ -84,6 +84,39 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Like mbar_wait_bounded, for a warp that usually waits long (the stream
+// kernels' producer, which waits most of a chunk for the consumers to
+// release a stage): it sleeps nap_ns between non-blocking tests, so its
+// polling takes few issue slots from the warps sharing its scheduler.
+__device__ __forceinline__ bool mbar_wait_napping(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns, volatile int* abort_flag,
+                                                  uint32_t nap_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    __nanosleep(nap_ns);
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
+  return false;
+}
+
 // Global -> shared bulk copy; completion is signalled on `bar` in bytes.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, uint32_t bytes,
