@@ -426,7 +426,7 @@ def run_extras(blk, peak, dev, reps=20, spmm_tile_n=0):
     launch), the convergence
     diagnostics (6.5 B/weight: logits and previous draws in, draws out) and
     the forward with the diagnostics in the same pass (10.5 B/weight), each
-    over all matrices (one launch per matrix), CUDA-event timed."""
+    over all matrices in one batched launch, CUDA-event timed."""
     import torch
     mk, wl = blk.mk, blk.wl
     L = mk.lib()
@@ -445,25 +445,25 @@ def run_extras(blk, peak, dev, reps=20, spmm_tile_n=0):
         st = L.maskllm_prior_from_mask_batched(pfm_arr, len(blk.mats), 1.0, 0.0, s)
         assert st == 0
 
+    # the diagnostics over the block: one batched launch per call
+    ms_arr = mk.matrix_array([{"W": None, "logits": m["logits"], "tensor_id": m["tensor_id"],
+                               "prev_idx": draws[i], "idx_out": nxt[i], "l1_row_out": l1[i],
+                               "maxprob_row_out": mp[i]} for i, m in enumerate(blk.mats)])
+
     def mask_stats(step):
-        for i, m in enumerate(blk.mats):
-            st = L.maskllm_mask_stats(m["logits"].data_ptr(), draws[i].data_ptr(), m["x"].rows,
-                                      m["x"].cols, wl.tau, wl.kappa,
-                                      mk.maskllm_rng(0, step, m["tensor_id"]), nxt[i].data_ptr(),
-                                      l1[i].data_ptr(), mp[i].data_ptr(), s)
-            assert st == 0
+        st = L.maskllm_mask_stats_batched(ms_arr, len(blk.mats), wl.tau, wl.kappa, 0, step, s)
+        assert st == 0
 
     w_out = [torch.empty_like(m["x"].W) for m in blk.mats]
     row_sq = [torch.empty((m["x"].rows,), dtype=torch.float32, device=dev) for m in blk.mats]
+    fs_arr = mk.matrix_array([{"W": m["W"], "logits": m["logits"], "tensor_id": m["tensor_id"],
+                               "prev_idx": draws[i], "W_out": w_out[i], "row_sq_out": row_sq[i],
+                               "idx_out": nxt[i], "l1_row_out": l1[i], "maxprob_row_out": mp[i]}
+                              for i, m in enumerate(blk.mats)])
 
     def forward_stats(step):
-        for i, m in enumerate(blk.mats):
-            st = L.maskllm_forward_stats(m["W"].data_ptr(), m["logits"].data_ptr(),
-                                         draws[i].data_ptr(), m["x"].rows, m["x"].cols, wl.tau,
-                                         wl.kappa, mk.maskllm_rng(0, step, m["tensor_id"]),
-                                         w_out[i].data_ptr(), row_sq[i].data_ptr(),
-                                         nxt[i].data_ptr(), l1[i].data_ptr(), mp[i].data_ptr(), s)
-            assert st == 0
+        st = L.maskllm_forward_stats_batched(fs_arr, len(blk.mats), wl.tau, wl.kappa, 0, step, s)
+        assert st == 0
 
     out = {}
     for name, fn, bpw in (("prior_from_mask", lambda i: prior_from_mask(), 6.125),
@@ -483,7 +483,7 @@ def run_extras(blk, peak, dev, reps=20, spmm_tile_n=0):
         gbs = bpw * blk.weights / sec / 1e9
         out[name] = {"us_per_block": round(sec * 1e6, 2), "GB_per_s": round(gbs, 1),
                      "frac_of_hbm": round(gbs / peak, 4), "bytes_per_weight": bpw,
-                     "launches_per_block": 1 if name == "prior_from_mask" else len(blk.mats)}
+                     "launches_per_block": -(-len(blk.mats) // mk.MAX_BATCH)}
     out["perm_search"] = run_perm_search(blk, dev)
     blk.mk.maskllm_test_spmm_tile_n(spmm_tile_n)
     try:

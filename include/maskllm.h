@@ -344,8 +344,9 @@ maskllm_status maskllm_perm_search_static(const uint16_t* W, int64_t rows, int64
  * maskllm_mask_stats for the same step; row_sq_out and maxprob_row_out are
  * the same row sums added in another order (they agree to about 1e-6
  * relative).  The noisy logits z the forward forms give the draws, so the
- * diagnostics cost no second pass over the logits: 0.5 bytes of traffic per
- * group more than the forward (the draws out, the previous draws in).
+ * diagnostics cost no second pass over the logits: 2 bytes of traffic per
+ * group (0.5 per weight) more than the forward (the draws out, the previous
+ * draws in).
  *   W, logits, W_out, row_sq_out   as maskllm_forward (row_sq_out nullable)
  *   prev_idx, idx_out, l1_row_out, maxprob_row_out   as maskllm_mask_stats
  *                                  (all nullable; l1_row_out needs prev_idx)
@@ -385,6 +386,10 @@ typedef struct {
   uint8_t* idx_out;           /* hard_compress output, nullable */
   const uint32_t* meta;       /* prior_from_mask input: 4-bit codes u32 [rows, cols/32]
                                  (logits_out is its output; W is not read) */
+  const uint8_t* prev_idx;    /* mask_stats, forward_stats input: the previous step's
+                                 draws, u8 [rows, cols/4], nullable */
+  uint32_t* l1_row_out;       /* mask_stats, forward_stats output, nullable (needs prev_idx) */
+  float* maxprob_row_out;     /* mask_stats, forward_stats output, nullable */
 } maskllm_matrix;
 
 /* n >= 1 matrices; the noise of matrix i uses (seed, step, mats[i].tensor_id). */
@@ -402,6 +407,17 @@ maskllm_status maskllm_hard_compress_batched(const maskllm_matrix* mats, int32_t
  * logits_out of every matrix; high and low as in the single call. */
 maskllm_status maskllm_prior_from_mask_batched(const maskllm_matrix* mats, int32_t n, float high,
                                                float low, maskllm_stream_t stream);
+/* maskllm_mask_stats over a batch (MaskLLM Fig. 5): reads logits and
+ * prev_idx, writes idx_out (the draws), l1_row_out and maxprob_row_out of
+ * every matrix; W is not read (rows and cols still describe the matrix). */
+maskllm_status maskllm_mask_stats_batched(const maskllm_matrix* mats, int32_t n, float tau,
+                                          float kappa, uint64_t seed, uint32_t step,
+                                          maskllm_stream_t stream);
+/* maskllm_forward_stats over a batch: reads W, logits and prev_idx, writes
+ * W_out, row_sq_out, idx_out (the draws), l1_row_out and maxprob_row_out. */
+maskllm_status maskllm_forward_stats_batched(const maskllm_matrix* mats, int32_t n, float tau,
+                                             float kappa, uint64_t seed, uint32_t step,
+                                             maskllm_stream_t stream);
 
 /* ---- Failure detection -------------------------------------------------
  * The pipelined kernels wait on shared-memory barriers for their bulk copies.

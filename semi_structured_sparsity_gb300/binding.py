@@ -29,7 +29,8 @@ EXPORTS = ("maskllm_prior_init", "maskllm_forward", "maskllm_backward",
            "maskllm_prior_from_mask_batched", "maskllm_mask_stats",
            "maskllm_perm_shift", "maskllm_perm_metric", "maskllm_permute_columns",
            "maskllm_perm_swap_gains", "maskllm_perm_search", "maskllm_perm_search_static",
-           "maskllm_spmm", "maskllm_forward_stats",
+           "maskllm_spmm", "maskllm_forward_stats", "maskllm_mask_stats_batched",
+           "maskllm_forward_stats_batched",
            "maskllm_set_wait_timeout",
            "maskllm_test_withhold_loads", "maskllm_test_spmm_tile_n", "maskllm_device_status",
            "maskllm_status_string",
@@ -50,7 +51,8 @@ class maskllm_matrix(C.Structure):
                 ("logits_out", C.c_void_p), ("W_out", C.c_void_p), ("row_sq_out", C.c_void_p),
                 ("probs_out", C.c_void_p), ("dlogits_out", C.c_void_p),
                 ("values_out", C.c_void_p), ("meta_out", C.c_void_p), ("idx_out", C.c_void_p),
-                ("meta", C.c_void_p)]
+                ("meta", C.c_void_p), ("prev_idx", C.c_void_p), ("l1_row_out", C.c_void_p),
+                ("maxprob_row_out", C.c_void_p)]
 
 
 class MaskLLMError(RuntimeError):
@@ -100,6 +102,8 @@ def lib() -> C.CDLL:
         L.maskllm_spmm.argtypes = [vp, vp, i64, i64, vp, i64, vp, vp]
         L.maskllm_forward_stats.argtypes = [vp, vp, vp, i64, i64, f32, f32, maskllm_rng, vp, vp,
                                             vp, vp, vp, vp]
+        L.maskllm_mask_stats_batched.argtypes = [mp, i32, f32, f32, u64, u32, vp]
+        L.maskllm_forward_stats_batched.argtypes = [mp, i32, f32, f32, u64, u32, vp]
         for fn in EXPORTS[:-3]:
             getattr(L, fn).restype = st
         L.maskllm_perm_workspace_bytes.argtypes = [i64, i64]
@@ -248,7 +252,8 @@ def maskllm_status_string(status: int) -> str:
 # ---------------------------------------------------------------------------
 
 _TENSOR_FIELDS = ("W", "logits", "grad_W_out", "logits_out", "W_out", "row_sq_out",
-                  "probs_out", "dlogits_out", "values_out", "meta_out", "idx_out", "meta")
+                  "probs_out", "dlogits_out", "values_out", "meta_out", "idx_out", "meta",
+                  "prev_idx", "l1_row_out", "maxprob_row_out")
 
 
 def matrix_array(mats):
@@ -261,6 +266,12 @@ def matrix_array(mats):
                     and meta.dim() == 2):
                 raise ValueError("meta must be a 2-D int32 CUDA tensor")
             a.rows, a.cols = meta.shape[0], 32 * meta.shape[1]
+        elif W is None and m.get("logits") is not None:
+            lg = m["logits"]
+            if not (isinstance(lg, torch.Tensor) and lg.dtype == torch.float32
+                    and lg.dim() == 3 and lg.shape[2] == 6):
+                raise ValueError("logits must be a float32 CUDA tensor [rows, cols/4, 6]")
+            a.rows, a.cols = lg.shape[0], 4 * lg.shape[1]
         else:
             if not (isinstance(W, torch.Tensor) and W.is_cuda and W.dtype == torch.bfloat16
                     and W.dim() == 2 and W.is_contiguous()):
@@ -304,6 +315,24 @@ def maskllm_prior_from_mask_batched(mats, high, low, stream=None):
     arr = matrix_array(mats)
     _check("maskllm_prior_from_mask_batched", lib().maskllm_prior_from_mask_batched(
         arr, len(mats), high, low, _stream(stream)))
+
+
+def maskllm_mask_stats_batched(mats, tau, kappa, seed, step, stream=None):
+    """maskllm_mask_stats over a batch: per matrix `logits`, `prev_idx` (u8
+    [rows, cols/4], optional) in; `idx_out`, `l1_row_out` (int32 [rows],
+    needs prev_idx), `maxprob_row_out` (fp32 [rows]) out, all optional."""
+    arr = matrix_array(mats)
+    _check("maskllm_mask_stats_batched", lib().maskllm_mask_stats_batched(
+        arr, len(mats), tau, kappa, seed, step, _stream(stream)))
+
+
+def maskllm_forward_stats_batched(mats, tau, kappa, seed, step, stream=None):
+    """maskllm_forward_stats over a batch: the forward's fields (`W`,
+    `logits`, `W_out`, `row_sq_out`) and the diagnostics' fields of
+    maskllm_mask_stats_batched."""
+    arr = matrix_array(mats)
+    _check("maskllm_forward_stats_batched", lib().maskllm_forward_stats_batched(
+        arr, len(mats), tau, kappa, seed, step, _stream(stream)))
 
 
 def maskllm_set_wait_timeout(nanoseconds: int) -> None:

@@ -43,15 +43,25 @@ bool overlaps(Span a, Span b) {
   return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
 }
 
-// Inputs and outputs of one call (all matrices of a batch together).
+// Inputs and outputs of one call (all matrices of a batch together; at most
+// 3 inputs and 5 outputs per matrix: the forward with diagnostics).
 struct Spans {
-  Span in[3 * kMaxBatch];
-  Span out[3 * kMaxBatch];
+  static constexpr int kCap = 8 * kMaxBatch;
+  Span in[kCap];
+  Span out[kCap];
   int n_in = 0, n_out = 0;
-  void input(const void* p, uint64_t b) { in[n_in++] = {p, b}; }
-  void output(const void* p, uint64_t b) { out[n_out++] = {p, b}; }
+  bool full = false;
+  void input(const void* p, uint64_t b) {
+    if (n_in < kCap) in[n_in++] = {p, b};
+    else full = true;
+  }
+  void output(const void* p, uint64_t b) {
+    if (n_out < kCap) out[n_out++] = {p, b};
+    else full = true;
+  }
   // Outputs must not overlap inputs nor each other.
   maskllm_status check() const {
+    if (full) return MASKLLM_ERR_INVALID_ARG;
     for (int o = 0; o < n_out; ++o) {
       for (int i = 0; i < n_in; ++i)
         if (overlaps(out[o], in[i])) return MASKLLM_ERR_ALIAS;
@@ -159,9 +169,48 @@ maskllm_status check_prior_from_mask(const maskllm_matrix& m, Spans& sp) {
   return MASKLLM_OK;
 }
 
+// The diagnostics' rules (maskllm_mask_stats): optional outputs, the L1
+// distance needs the previous draws, rows no longer than 2^24 weights.
+maskllm_status check_diagnostics(const maskllm_matrix& m, Spans& sp) {
+  MK_TRY(check_optional(m.prev_idx));
+  MK_TRY(check_optional(m.idx_out));
+  MK_TRY(check_optional(m.l1_row_out));
+  MK_TRY(check_optional(m.maxprob_row_out));
+  if (m.l1_row_out != nullptr && m.prev_idx == nullptr) return MASKLLM_ERR_INVALID_ARG;
+  MK_TRY(check_shape(m.rows, m.cols));
+  if (m.cols > (int64_t(1) << 24)) return MASKLLM_ERR_SHAPE;
+  const uint64_t n = weights(m), r4 = 4 * static_cast<uint64_t>(m.rows);
+  sp.input(m.prev_idx, n / 4);
+  sp.output(m.idx_out, n / 4);
+  sp.output(m.l1_row_out, r4);
+  sp.output(m.maxprob_row_out, r4);
+  return MASKLLM_OK;
+}
+
+maskllm_status check_mask_stats(const maskllm_matrix& m, Spans& sp) {
+  const void* ptrs[] = {m.logits};
+  MK_TRY(check_ptrs(ptrs, 1));
+  MK_TRY(check_diagnostics(m, sp));
+  sp.input(m.logits, 6 * weights(m));
+  return MASKLLM_OK;
+}
+
+maskllm_status check_forward_stats(const maskllm_matrix& m, Spans& sp) {
+  const void* ptrs[] = {m.W, m.logits, m.W_out};
+  MK_TRY(check_ptrs(ptrs, 3));
+  MK_TRY(check_optional(m.row_sq_out));
+  MK_TRY(check_diagnostics(m, sp));
+  const uint64_t n = weights(m);
+  sp.input(m.W, 2 * n);
+  sp.input(m.logits, 6 * n);
+  sp.output(m.W_out, 2 * n);
+  sp.output(m.row_sq_out, 4 * static_cast<uint64_t>(m.rows));
+  return MASKLLM_OK;
+}
+
 maskllm_status finish(cudaError_t e) { return e == cudaSuccess ? MASKLLM_OK : cuda_fail(e); }
 
-enum class Op { kPrior, kForward, kBackward, kCompress, kPriorFromMask };
+enum class Op { kPrior, kForward, kBackward, kCompress, kPriorFromMask, kMaskStats, kForwardStats };
 
 struct Call {
   Op op;
@@ -197,6 +246,21 @@ StreamMatrix to_stream(const maskllm_matrix& m, Op op) {
       s.G = nullptr;
       s.out0 = m.logits_out;
       break;
+    case Op::kMaskStats:
+      s.W = nullptr;
+      s.G = m.prev_idx;
+      s.out0 = m.idx_out;
+      s.out1 = m.l1_row_out;
+      s.out2 = m.maxprob_row_out;
+      break;
+    case Op::kForwardStats:
+      s.G = m.prev_idx;
+      s.out0 = m.W_out;
+      s.out1 = m.row_sq_out;
+      s.out2 = m.idx_out;
+      s.out3 = m.l1_row_out;
+      s.out4 = m.maxprob_row_out;
+      break;
   }
   return s;
 }
@@ -209,13 +273,17 @@ maskllm_status check_matrix(Op op, const maskllm_matrix& m, Spans& sp) {
     case Op::kBackward: return check_backward(m, sp);
     case Op::kCompress: return check_compress(m, sp);
     case Op::kPriorFromMask: return check_prior_from_mask(m, sp);
+    case Op::kMaskStats: return check_mask_stats(m, sp);
+    case Op::kForwardStats: return check_forward_stats(m, sp);
   }
   return MASKLLM_ERR_INVALID_ARG;
 }
 
 maskllm_status run(const Call& c, const maskllm_matrix* mats, int32_t n, cudaStream_t s) {
   if (mats == nullptr || n < 1) return MASKLLM_ERR_INVALID_ARG;
-  if (c.op == Op::kForward || c.op == Op::kBackward) MK_TRY(check_temperature(c.tau, c.kappa));
+  if (c.op == Op::kForward || c.op == Op::kBackward || c.op == Op::kMaskStats ||
+      c.op == Op::kForwardStats)
+    MK_TRY(check_temperature(c.tau, c.kappa));
   if (!isfinite(c.reg) || !isfinite(c.scale) || !isfinite(c.high) || !isfinite(c.low))
     return MASKLLM_ERR_INVALID_ARG;
   // validate everything before launching anything
@@ -261,6 +329,8 @@ maskllm_status run(const Call& c, const maskllm_matrix* mats, int32_t n, cudaStr
       case Op::kBackward: e = stream_backward(d, sm, nb, c.tau, c.kappa, rng, c.reg, s); break;
       case Op::kCompress: e = stream_hard_compress(d, sm, nb, s); break;
       case Op::kPriorFromMask: e = launch_prior_from_mask(d, sm, nb, c.high, c.low, s); break;
+      case Op::kMaskStats: e = stream_mask_stats(d, sm, nb, c.tau, c.kappa, rng, s); break;
+      case Op::kForwardStats: e = stream_forward_stats(d, sm, nb, c.tau, c.kappa, rng, s); break;
     }
     if (e != cudaSuccess) return cuda_fail(e);
   }
@@ -444,6 +514,28 @@ maskllm_status maskllm_prior_from_mask_batched(const maskllm_matrix* mats, int32
   Call c{Op::kPriorFromMask};
   c.high = high;
   c.low = low;
+  return maskllm::run(c, mats, n, stream);
+}
+
+maskllm_status maskllm_mask_stats_batched(const maskllm_matrix* mats, int32_t n, float tau,
+                                          float kappa, uint64_t seed, uint32_t step,
+                                          maskllm_stream_t stream) {
+  Call c{Op::kMaskStats};
+  c.tau = tau;
+  c.kappa = kappa;
+  c.seed = seed;
+  c.step = step;
+  return maskllm::run(c, mats, n, stream);
+}
+
+maskllm_status maskllm_forward_stats_batched(const maskllm_matrix* mats, int32_t n, float tau,
+                                             float kappa, uint64_t seed, uint32_t step,
+                                             maskllm_stream_t stream) {
+  Call c{Op::kForwardStats};
+  c.tau = tau;
+  c.kappa = kappa;
+  c.seed = seed;
+  c.step = step;
   return maskllm::run(c, mats, n, stream);
 }
 

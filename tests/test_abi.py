@@ -166,6 +166,50 @@ def test_prior_from_mask_batched_validation(L):
     assert L.maskllm_prior_from_mask_batched(arr, 2, 1.0, 0.0, None) == SHAPE
 
 
+def test_diagnostics_batched_validation(L):
+    from semi_structured_sparsity_gb300 import binding
+    arr = (binding.maskllm_matrix * 2)()
+    arr[0] = _mat(logits=A, idx_out=B)
+    arr[1] = _mat(logits=D, maxprob_row_out=E)
+    for fn in (L.maskllm_mask_stats_batched, L.maskllm_forward_stats_batched):
+        assert fn(arr, 0, 1.0, 1.0, 0, 0, None) == INVALID
+        assert fn(None, 1, 1.0, 1.0, 0, 0, None) == INVALID
+        assert fn(arr, 2, 0.0, 1.0, 0, 0, None) == INVALID              # tau <= 0
+        assert fn(arr, 2, 1.0, float("inf"), 0, 0, None) == INVALID     # kappa not finite
+    # the L1 distance needs the previous draws
+    arr[1] = _mat(logits=D, l1_row_out=E)
+    assert L.maskllm_mask_stats_batched(arr, 2, 1.0, 1.0, 0, 0, None) == INVALID
+    arr[1].prev_idx = Cc
+    arr[1].l1_row_out = Cc + 4                # misaligned output
+    assert L.maskllm_mask_stats_batched(arr, 2, 1.0, 1.0, 0, 0, None) == ALIGN
+    arr[1].l1_row_out = A + 32                # writes over matrix 0's logits
+    assert L.maskllm_mask_stats_batched(arr, 2, 1.0, 1.0, 0, 0, None) == ALIAS
+    arr[1] = _mat(logits=D, maxprob_row_out=E, rows=1, cols=(1 << 24) + 32)
+    assert L.maskllm_mask_stats_batched(arr, 2, 1.0, 1.0, 0, 0, None) == SHAPE
+    # the fused pass also needs W and W_out
+    arr[1] = _mat(logits=D, maxprob_row_out=E)
+    assert L.maskllm_forward_stats_batched(arr, 2, 1.0, 1.0, 0, 0, None) == INVALID
+    arr[0] = _mat(W=0x700000, logits=A, W_out=0x710000, idx_out=B)
+    arr[1] = _mat(W=0x720000, logits=D, W_out=0x730000, row_sq_out=0x730000 + 16)
+    assert L.maskllm_forward_stats_batched(arr, 2, 1.0, 1.0, 0, 0, None) == ALIAS
+
+
+def test_full_batch_of_fused_diagnostics_validates_every_span(L):
+    # 16 matrices x (3 inputs + 5 outputs): validation records every span
+    # and finds the alias between the last matrix and the first
+    from semi_structured_sparsity_gb300 import binding
+    n = binding.MAX_BATCH
+    arr = (binding.maskllm_matrix * n)()
+    base = 0x10000000
+    for i in range(n):
+        o = base + i * 0x100000
+        arr[i] = _mat(W=o, logits=o + 0x1000, prev_idx=o + 0x2000, W_out=o + 0x3000,
+                      row_sq_out=o + 0x4000, idx_out=o + 0x5000, l1_row_out=o + 0x6000,
+                      maxprob_row_out=o + 0x7000)
+    arr[n - 1].maxprob_row_out = base + 0x3000   # over matrix 0's W_out
+    assert L.maskllm_forward_stats_batched(arr, n, 1.0, 1.0, 0, 0, None) == ALIAS
+
+
 def test_next_entry_points_validation(L):
     r = _rng()
     assert L.maskllm_prior_from_mask(A, 4, 64, float("inf"), 0.0, B, None) == INVALID

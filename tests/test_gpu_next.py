@@ -145,6 +145,56 @@ def test_forward_stats_is_forward_plus_stats(rows, cols, tau, kappa):
     assert_close(mp.cpu().numpy(), wmp, rtol=1e-5, atol=0, what="max-probability row sum")
 
 
+@pytest.mark.parametrize("n", [len(SHAPES), 20])
+def test_diagnostics_batched_match_single_calls_and_oracle(n):
+    """maskllm_mask_stats_batched and maskllm_forward_stats_batched over
+    matrices of every test shape (long rows, rows shorter than a chunk,
+    ragged last chunks), each with its own tensor id: every output
+    bit-identical to the single-matrix call, draws and L1 to the oracle; 20
+    matrices take two launches."""
+    tau, kappa, seed, step = 0.5, 40.0, 9, 21
+    shapes = [SHAPES[i % len(SHAPES)] for i in range(n)]
+    mats, fmats = [], []
+    for i, (rows, cols) in enumerate(shapes):
+        W, L, _ = wl.random_case(rows, cols, seed=700 + i, device="cuda")
+        tid = 3 + i
+        prev, _, _ = mk.maskllm_mask_stats(L, tau, kappa, (seed, step - 1, tid))
+        g = cols // 4
+        mats.append({"W": None, "logits": L, "tensor_id": tid, "prev_idx": prev,
+                     "idx_out": torch.empty((rows, g), dtype=torch.uint8, device="cuda"),
+                     "l1_row_out": torch.empty((rows,), dtype=torch.int32, device="cuda"),
+                     "maxprob_row_out": torch.empty((rows,), device="cuda")})
+        fmats.append({"W": W, "logits": L, "tensor_id": tid, "prev_idx": prev,
+                      "W_out": torch.empty_like(W),
+                      "row_sq_out": torch.empty((rows,), device="cuda"),
+                      "idx_out": torch.empty((rows, g), dtype=torch.uint8, device="cuda"),
+                      "l1_row_out": torch.empty((rows,), dtype=torch.int32, device="cuda"),
+                      "maxprob_row_out": torch.empty((rows,), device="cuda")})
+    mk.maskllm_mask_stats_batched(mats, tau, kappa, seed, step)
+    mk.maskllm_forward_stats_batched(fmats, tau, kappa, seed, step)
+    torch.cuda.synchronize()
+    for (rows, cols), m, f in zip(shapes, mats, fmats):
+        rng = (seed, step, m["tensor_id"])
+        idx, l1, mp = mk.maskllm_mask_stats(m["logits"], tau, kappa, rng, prev_idx=m["prev_idx"])
+        Wo, rsq, fidx, fl1, fmp = mk.maskllm_forward_stats(f["W"], f["logits"], tau, kappa, rng,
+                                                           prev_idx=f["prev_idx"])
+        torch.cuda.synchronize()
+        assert torch.equal(m["idx_out"], idx) and torch.equal(m["l1_row_out"], l1)
+        assert torch.equal(m["maxprob_row_out"].view(torch.int32), mp.view(torch.int32))
+        assert torch.equal(f["W_out"].view(torch.int16), Wo.view(torch.int16))
+        assert torch.equal(f["row_sq_out"].view(torch.int32), rsq.view(torch.int32))
+        assert torch.equal(f["idx_out"], fidx) and torch.equal(f["l1_row_out"], fl1)
+        assert torch.equal(f["maxprob_row_out"].view(torch.int32), fmp.view(torch.int32))
+        Lh = m["logits"].cpu().numpy()
+        wprev, _, _ = orc.mask_stats(Lh, rows, cols, tau, kappa, seed, step - 1, m["tensor_id"])
+        widx, wl1, wmp = orc.mask_stats(Lh, rows, cols, tau, kappa, *rng, prev_idx=wprev)
+        assert_bits_equal(m["idx_out"].cpu().numpy(), widx, "batched draws")
+        assert_bits_equal(m["l1_row_out"].cpu().numpy().view(np.uint32), wl1.astype(np.uint32),
+                          "batched L1 per row")
+        assert_close(m["maxprob_row_out"].cpu().numpy(), wmp, rtol=1e-5, atol=0,
+                     what="batched max-probability row sum")
+
+
 def test_forward_stats_optional_outputs():
     W, L, _ = wl.random_case(40, 256, seed=5, device="cuda")
     Wo, rsq, idx, l1, mp = mk.maskllm_forward_stats(W, L, 1.0, 3.0, (1, 2, 3), want_row_sq=False,
