@@ -339,11 +339,11 @@ maskllm_status maskllm_perm_search_static(const uint16_t* W, int64_t rows, int64
                                           int32_t* shift_out, maskllm_stream_t stream);
 
 /* The forward and the convergence diagnostics of one step in a single pass
- * (MaskLLM Fig. 5; the optional outputs of maskllm_forward): W_out, idx_out
- * and l1_row_out are bit-identical to those of maskllm_forward and
- * maskllm_mask_stats for the same step; row_sq_out and maxprob_row_out are
- * the same row sums added in another order (they agree to about 1e-6
- * relative).  The noisy logits z the forward forms give the draws, so the
+ * (MaskLLM Fig. 5; the optional outputs of maskllm_forward): every output
+ * is bit-identical to that of maskllm_forward (W_out, row_sq_out) or
+ * maskllm_mask_stats (idx_out, l1_row_out, maxprob_row_out) for the same
+ * step: the row sums are added in the same order.  The noisy logits z the
+ * forward forms give the draws, so the
  * diagnostics cost no second pass over the logits: 2 bytes of traffic per
  * group (0.5 per weight) more than the forward (the draws out, the previous
  * draws in).

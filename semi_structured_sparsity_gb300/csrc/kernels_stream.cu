@@ -302,10 +302,6 @@ struct OpBase {
   // every thread leaves its own partial and the producer adds kConsumers
   static constexpr bool kWarpRowSums = false;
   static constexpr int kIntQuantity = -1;   // row quantity summed as an integer (none)
-  // the consumers write row partials into bytes the next copy overwrites
-  // (their consumed W slots): the producer orders those generic-proxy
-  // accesses before its async-proxy copies with a proxy fence
-  static constexpr bool kPartialsInCopyTarget = false;
   // chunk the matrices flat (no per-row sums: prior, backward, compress)
   static constexpr bool kFlat = false;
   // staged outputs: buffers per stage (chunk n of a stage's ring writes
@@ -676,19 +672,25 @@ struct StatsOp : OpBase<GPT, 4> {
 // the forward forms anyway give the draw (their first maximum), and the
 // scaled logits fl32(kappa * L) it forms on the way give the distribution's
 // largest probability.  W' is computed exactly as in FwdOp, the draws and
-// the L1 distances exactly as in StatsOp; the row sums of squares and of
-// the maximum probabilities are the same sums added in this op's own order
-// (per-thread partials, in the thread's consumed W slot).  Row quantities:
-// 0 row_sq, 1 L1 distance, 2 max-probability sum.
+// the L1 distances exactly as in StatsOp, and the row sums are added in
+// their order too (each thread's groups in turn, warp sums, the producer
+// adding the 16 warp sums).  Row quantities: 0 row_sq, 1 L1 distance, 2
+// max-probability sum.
 template <int GPT>
 struct FwdStatsOp : OpBase<GPT, 4> {
   static constexpr bool kTable = true, kStaged = false, kWarpWide = false;
   static constexpr bool kOutOverlapsInput = false;
   static constexpr int kRowQuantities = 3;
-  static constexpr uint32_t kPartOffset = 0;
-  static constexpr uint32_t kPartStride = 8 * GPT;
-  static_assert(8 * GPT >= 12, "three row partials fit the thread's W slot");
-  static constexpr bool kPartialsInCopyTarget = true;
+  // warp sums in a region of their own after the logits, the refill issued
+  // before the producer adds them: 584 -> 536 us on the LLaMA-2-7B block
+  // (rows of 1024 groups end a row every chunk), a Nemotron-4 layer 1012 ->
+  // 1039 us (a row end every other chunk); per-thread partials summed by the
+  // producer after its refill: 613 and 980 us
+  static constexpr bool kWarpRowSums = true;
+  static constexpr int kIntQuantity = 1;   // the L1 distance is an integer count
+  static constexpr bool kRefillFirst = true;
+  static constexpr uint32_t kPartOffset = kChunkGroups * (8 + 24);
+  static constexpr uint32_t kPartStride = 12;
   __device__ static bool want_row(const MatDesc& d, int q) {
     return q == 0 ? d.out1 != nullptr : (q == 1 ? (d.out3 != nullptr && d.G != nullptr)
                                                  : d.out4 != nullptr);
@@ -701,7 +703,7 @@ struct FwdStatsOp : OpBase<GPT, 4> {
     else
       static_cast<float*>(d.out4)[row] = v;
   }
-  static constexpr uint32_t kStageBytes = kChunkGroups * (8 + 24);
+  static constexpr uint32_t kStageBytes = kPartOffset + (kChunkGroups / GPT) * kPartStride;
   static constexpr uint32_t kOutOffset = 0;
   static constexpr uint32_t kOutBytesPerGroup = 0;
 
@@ -876,7 +878,6 @@ __device__ void producer(const StreamParams& p, uint8_t* smem, int64_t u0, int64
       // a staged store may still be reading this stage's output region:
       // wait before the refill if the copies land there, after it if not
       if (Op::kStaged && Op::kOutOverlapsInput) bulk_wait_reads();
-      if (Op::kPartialsInCopyTarget) fence_proxy_async_smem();
       if (!p.withhold_loads)
         Op::issue(p.mats[c.mat], c, stages + s * Op::kStageBytes, &full[s]);
       else
