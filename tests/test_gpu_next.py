@@ -196,6 +196,54 @@ def test_diagnostics_batched_match_single_calls_and_oracle(n):
                      what="batched max-probability row sum")
 
 
+def test_diagnostics_batched_optional_outputs_per_matrix():
+    """A batch whose matrices leave out different optional outputs (no
+    previous draws and no L1, no draws, no max probability, no row sums):
+    what each writes equals the single call's bit for bit."""
+    tau, kappa, seed, step = 1.0, 3.0, 4, 9
+    shapes = [(7, 160), (300, 64), (5, 4128), (33, 11008)]
+    mats, fmats, want = [], [], []
+    for i, (rows, cols) in enumerate(shapes):
+        W, L, _ = wl.random_case(rows, cols, seed=800 + i, device="cuda")
+        g = cols // 4
+        prev = None if i == 0 else mk.maskllm_mask_stats(L, tau, kappa, (seed, step - 1, i))[0]
+        m = {"W": None, "logits": L, "tensor_id": i, "prev_idx": prev,
+             "idx_out": None if i == 1 else torch.full((rows, g), 255, dtype=torch.uint8,
+                                                       device="cuda"),
+             "l1_row_out": None if prev is None else torch.full((rows,), -1, dtype=torch.int32,
+                                                                device="cuda"),
+             "maxprob_row_out": None if i == 2 else torch.full((rows,), -1.0, device="cuda")}
+        f = dict(m, W=W, W_out=torch.empty_like(W),
+                 row_sq_out=None if i == 3 else torch.empty((rows,), device="cuda"),
+                 idx_out=None if m["idx_out"] is None else torch.empty_like(m["idx_out"]),
+                 l1_row_out=None if m["l1_row_out"] is None else torch.empty_like(m["l1_row_out"]),
+                 maxprob_row_out=(None if m["maxprob_row_out"] is None
+                                  else torch.empty_like(m["maxprob_row_out"])))
+        mats.append(m)
+        fmats.append(f)
+        want.append((L, W, prev))
+    mk.maskllm_mask_stats_batched(mats, tau, kappa, seed, step)
+    mk.maskllm_forward_stats_batched(fmats, tau, kappa, seed, step)
+    torch.cuda.synchronize()
+    for i, (m, f, (L, W, prev)) in enumerate(zip(mats, fmats, want)):
+        rng = (seed, step, i)
+        idx, l1, mp = mk.maskllm_mask_stats(L, tau, kappa, rng, prev_idx=prev)
+        Wo, rsq, _, _, _ = mk.maskllm_forward_stats(W, L, tau, kappa, rng, prev_idx=prev)
+        torch.cuda.synchronize()
+        for out, ref in ((m["idx_out"], idx), (f["idx_out"], idx)):
+            if out is not None:
+                assert torch.equal(out, ref)
+        for out, ref in ((m["l1_row_out"], l1), (f["l1_row_out"], l1)):
+            if out is not None:
+                assert torch.equal(out, ref)
+        for out, ref in ((m["maxprob_row_out"], mp), (f["maxprob_row_out"], mp)):
+            if out is not None:
+                assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+        assert torch.equal(f["W_out"].view(torch.int16), Wo.view(torch.int16))
+        if f["row_sq_out"] is not None:
+            assert torch.equal(f["row_sq_out"].view(torch.int32), rsq.view(torch.int32))
+
+
 def test_forward_stats_optional_outputs():
     W, L, _ = wl.random_case(40, 256, seed=5, device="cuda")
     Wo, rsq, idx, l1, mp = mk.maskllm_forward_stats(W, L, 1.0, 3.0, (1, 2, 3), want_row_sq=False,
