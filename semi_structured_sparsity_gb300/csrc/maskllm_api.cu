@@ -543,38 +543,21 @@ maskllm_status maskllm_mask_stats(const float* logits, const uint8_t* prev_idx, 
                                   int64_t cols, float tau, float kappa, maskllm_rng rng,
                                   uint8_t* idx_out, uint32_t* l1_row_out,
                                   float* maxprob_row_out, maskllm_stream_t stream) {
-  const void* ptrs[] = {logits};
-  MK_TRY(maskllm::check_ptrs(ptrs, 1));
-  MK_TRY(maskllm::check_optional(prev_idx));
-  MK_TRY(maskllm::check_optional(idx_out));
-  MK_TRY(maskllm::check_optional(l1_row_out));
-  MK_TRY(maskllm::check_optional(maxprob_row_out));
-  if (l1_row_out != nullptr && prev_idx == nullptr) return MASKLLM_ERR_INVALID_ARG;
-  MK_TRY(maskllm::check_shape(rows, cols));
-  if (cols > (int64_t(1) << 24)) return MASKLLM_ERR_SHAPE;
-  MK_TRY(maskllm::check_temperature(tau, kappa));
-  const uint64_t n = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols);
-  maskllm::Spans sp;
-  sp.input(logits, 6 * n);
-  sp.input(prev_idx, n / 4);
-  sp.output(idx_out, n / 4);
-  sp.output(l1_row_out, 4 * static_cast<uint64_t>(rows));
-  sp.output(maxprob_row_out, 4 * static_cast<uint64_t>(rows));
-  MK_TRY(sp.check());
-  maskllm::Device d;
-  cudaError_t e = maskllm::current_device(&d);
-  if (e != cudaSuccess) return maskllm::cuda_fail(e);
-  maskllm::StreamMatrix m{};
-  m.L = logits;
-  m.G = prev_idx;
-  m.out0 = idx_out;
-  m.out1 = l1_row_out;
-  m.out2 = maxprob_row_out;
+  maskllm_matrix m{};
+  m.logits = logits;
+  m.prev_idx = prev_idx;
   m.rows = rows;
   m.cols = cols;
   m.tensor_id = rng.tensor_id;
-  return maskllm::finish(maskllm::stream_mask_stats(d, &m, 1, tau, kappa,
-                                                    {rng.seed, rng.step, rng.tensor_id}, stream));
+  m.idx_out = idx_out;
+  m.l1_row_out = l1_row_out;
+  m.maxprob_row_out = maxprob_row_out;
+  Call c{Op::kMaskStats};
+  c.tau = tau;
+  c.kappa = kappa;
+  c.seed = rng.seed;
+  c.step = rng.step;
+  return maskllm::run(c, &m, 1, stream);
 }
 
 }  // extern "C"
@@ -711,46 +694,24 @@ maskllm_status maskllm_forward_stats(const uint16_t* W, const float* logits,
                                      float tau, float kappa, maskllm_rng rng, uint16_t* W_out,
                                      float* row_sq_out, uint8_t* idx_out, uint32_t* l1_row_out,
                                      float* maxprob_row_out, maskllm_stream_t stream) {
-  const void* ptrs[] = {W, logits, W_out};
-  MK_TRY(maskllm::check_ptrs(ptrs, 3));
-  MK_TRY(maskllm::check_optional(prev_idx));
-  MK_TRY(maskllm::check_optional(row_sq_out));
-  MK_TRY(maskllm::check_optional(idx_out));
-  MK_TRY(maskllm::check_optional(l1_row_out));
-  MK_TRY(maskllm::check_optional(maxprob_row_out));
-  if (l1_row_out != nullptr && prev_idx == nullptr) return MASKLLM_ERR_INVALID_ARG;
-  MK_TRY(maskllm::check_shape(rows, cols));
-  if (cols > (int64_t(1) << 24)) return MASKLLM_ERR_SHAPE;
-  MK_TRY(maskllm::check_temperature(tau, kappa));
-  const uint64_t n = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols);
-  const uint64_t r4 = 4 * static_cast<uint64_t>(rows);
-  maskllm::Spans sp;
-  sp.input(W, 2 * n);
-  sp.input(logits, 6 * n);
-  sp.input(prev_idx, n / 4);
-  sp.output(W_out, 2 * n);
-  sp.output(row_sq_out, r4);
-  sp.output(idx_out, n / 4);
-  sp.output(l1_row_out, r4);
-  sp.output(maxprob_row_out, r4);
-  MK_TRY(sp.check());
-  maskllm::Device d;
-  cudaError_t e = maskllm::current_device(&d);
-  if (e != cudaSuccess) return maskllm::cuda_fail(e);
-  maskllm::StreamMatrix m{};
+  maskllm_matrix m{};
   m.W = W;
-  m.L = logits;
-  m.G = prev_idx;
-  m.out0 = W_out;
-  m.out1 = row_sq_out;
-  m.out2 = idx_out;
-  m.out3 = l1_row_out;
-  m.out4 = maxprob_row_out;
+  m.logits = logits;
+  m.prev_idx = prev_idx;
   m.rows = rows;
   m.cols = cols;
   m.tensor_id = rng.tensor_id;
-  return maskllm::finish(maskllm::stream_forward_stats(
-      d, &m, 1, tau, kappa, {rng.seed, rng.step, rng.tensor_id}, stream));
+  m.W_out = W_out;
+  m.row_sq_out = row_sq_out;
+  m.idx_out = idx_out;
+  m.l1_row_out = l1_row_out;
+  m.maxprob_row_out = maxprob_row_out;
+  Call c{Op::kForwardStats};
+  c.tau = tau;
+  c.kappa = kappa;
+  c.seed = rng.seed;
+  c.step = rng.step;
+  return maskllm::run(c, &m, 1, stream);
 }
 
 maskllm_status maskllm_set_wait_timeout(uint64_t nanoseconds) {
