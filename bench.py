@@ -425,8 +425,9 @@ def run_extras(blk, peak, dev, reps=20, spmm_tile_n=0):
     from a given mask (6.125 B/weight: codes in, logits out; one batched
     launch), the convergence
     diagnostics (6.5 B/weight: logits and previous draws in, draws out) and
-    the forward with the diagnostics in the same pass (10.5 B/weight), each
-    over all matrices in one batched launch, CUDA-event timed."""
+    the forward with the diagnostics in the same pass (10.5 B/weight) and
+    the backward with them (16.5 B/weight), each over all matrices in one
+    batched launch, CUDA-event timed."""
     import torch
     mk, wl = blk.mk, blk.wl
     L = mk.lib()
@@ -465,10 +466,23 @@ def run_extras(blk, peak, dev, reps=20, spmm_tile_n=0):
         st = L.maskllm_forward_stats_batched(fs_arr, len(blk.mats), wl.tau, wl.kappa, 0, step, s)
         assert st == 0
 
+    # the backward with the diagnostics (dlogits into the step's own buffers)
+    bs_arr = mk.matrix_array([{"W": m["W"], "logits": m["logits"], "grad_W_out": m["grad_W_out"],
+                               "tensor_id": m["tensor_id"], "prev_idx": draws[i],
+                               "dlogits_out": m["dlogits_out"], "idx_out": nxt[i],
+                               "l1_row_out": l1[i], "maxprob_row_out": mp[i]}
+                              for i, m in enumerate(blk.mats)])
+
+    def backward_stats(step):
+        st = L.maskllm_backward_stats_batched(bs_arr, len(blk.mats), wl.tau, wl.kappa, 0, step,
+                                              0.0, s)
+        assert st == 0
+
     out = {}
     for name, fn, bpw in (("prior_from_mask", lambda i: prior_from_mask(), 6.125),
                           ("mask_stats", mask_stats, 6.5),
-                          ("forward_stats", forward_stats, 10.5)):
+                          ("forward_stats", forward_stats, 10.5),
+                          ("backward_stats", backward_stats, 16.5)):
         for i in range(3):
             fn(i)
         torch.cuda.synchronize(dev)

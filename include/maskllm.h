@@ -357,6 +357,25 @@ maskllm_status maskllm_forward_stats(const uint16_t* W, const float* logits,
                                      float* row_sq_out, uint8_t* idx_out, uint32_t* l1_row_out,
                                      float* maxprob_row_out, maskllm_stream_t stream);
 
+/* The backward and the convergence diagnostics of one step in a single pass
+ * (MaskLLM Fig. 5; the same quantities as maskllm_forward_stats, for a
+ * caller that wants them from the backward): every output is bit-identical
+ * to that of maskllm_backward (dlogits_out) or maskllm_mask_stats (idx_out,
+ * l1_row_out, maxprob_row_out) for the same step.  The backward regenerates
+ * the step's noisy logits z, which give the draws, so the diagnostics need
+ * no second pass over the logits: 2 bytes of traffic per group (0.5 per
+ * weight) more than the backward, and their arithmetic.
+ *   W, logits, grad_W_out, reg_coeff, dlogits_out   as maskllm_backward
+ *   prev_idx, idx_out, l1_row_out, maxprob_row_out   as maskllm_mask_stats
+ *                                  (all nullable; l1_row_out needs prev_idx)
+ * cols <= 2^24. */
+maskllm_status maskllm_backward_stats(const uint16_t* W, const float* logits,
+                                      const uint16_t* grad_W_out, const uint8_t* prev_idx,
+                                      int64_t rows, int64_t cols, float tau, float kappa,
+                                      maskllm_rng rng, float reg_coeff, float* dlogits_out,
+                                      uint8_t* idx_out, uint32_t* l1_row_out,
+                                      float* maxprob_row_out, maskllm_stream_t stream);
+
 /* ---- Batched calls ------------------------------------------------------
  * One launch processes up to MASKLLM_MAX_BATCH matrices (for example the
  * seven linears of a transformer block); longer lists are split into several
@@ -386,10 +405,10 @@ typedef struct {
   uint8_t* idx_out;           /* hard_compress output, nullable */
   const uint32_t* meta;       /* prior_from_mask input: 4-bit codes u32 [rows, cols/32]
                                  (logits_out is its output; W is not read) */
-  const uint8_t* prev_idx;    /* mask_stats, forward_stats input: the previous step's
-                                 draws, u8 [rows, cols/4], nullable */
-  uint32_t* l1_row_out;       /* mask_stats, forward_stats output, nullable (needs prev_idx) */
-  float* maxprob_row_out;     /* mask_stats, forward_stats output, nullable */
+  const uint8_t* prev_idx;    /* mask_stats, forward_stats, backward_stats input: the
+                                 previous step's draws, u8 [rows, cols/4], nullable */
+  uint32_t* l1_row_out;       /* diagnostics output, nullable (needs prev_idx) */
+  float* maxprob_row_out;     /* diagnostics output, nullable */
 } maskllm_matrix;
 
 /* n >= 1 matrices; the noise of matrix i uses (seed, step, mats[i].tensor_id). */
@@ -418,6 +437,12 @@ maskllm_status maskllm_mask_stats_batched(const maskllm_matrix* mats, int32_t n,
 maskllm_status maskllm_forward_stats_batched(const maskllm_matrix* mats, int32_t n, float tau,
                                              float kappa, uint64_t seed, uint32_t step,
                                              maskllm_stream_t stream);
+/* maskllm_backward_stats over a batch: reads W, logits, grad_W_out and
+ * prev_idx, writes dlogits_out, idx_out (the draws), l1_row_out and
+ * maxprob_row_out. */
+maskllm_status maskllm_backward_stats_batched(const maskllm_matrix* mats, int32_t n, float tau,
+                                              float kappa, uint64_t seed, uint32_t step,
+                                              float reg_coeff, maskllm_stream_t stream);
 
 /* ---- Failure detection -------------------------------------------------
  * The pipelined kernels wait on shared-memory barriers for their bulk copies.

@@ -30,7 +30,8 @@ EXPORTS = ("maskllm_prior_init", "maskllm_forward", "maskllm_backward",
            "maskllm_perm_shift", "maskllm_perm_metric", "maskllm_permute_columns",
            "maskllm_perm_swap_gains", "maskllm_perm_search", "maskllm_perm_search_static",
            "maskllm_spmm", "maskllm_forward_stats", "maskllm_mask_stats_batched",
-           "maskllm_forward_stats_batched",
+           "maskllm_forward_stats_batched", "maskllm_backward_stats",
+           "maskllm_backward_stats_batched",
            "maskllm_set_wait_timeout",
            "maskllm_test_withhold_loads", "maskllm_test_spmm_tile_n", "maskllm_device_status",
            "maskllm_status_string",
@@ -104,6 +105,9 @@ def lib() -> C.CDLL:
                                             vp, vp, vp, vp]
         L.maskllm_mask_stats_batched.argtypes = [mp, i32, f32, f32, u64, u32, vp]
         L.maskllm_forward_stats_batched.argtypes = [mp, i32, f32, f32, u64, u32, vp]
+        L.maskllm_backward_stats.argtypes = [vp, vp, vp, vp, i64, i64, f32, f32, maskllm_rng, f32,
+                                             vp, vp, vp, vp, vp]
+        L.maskllm_backward_stats_batched.argtypes = [mp, i32, f32, f32, u64, u32, f32, vp]
         for fn in EXPORTS[:-3]:
             getattr(L, fn).restype = st
         L.maskllm_perm_workspace_bytes.argtypes = [i64, i64]
@@ -335,6 +339,15 @@ def maskllm_forward_stats_batched(mats, tau, kappa, seed, step, stream=None):
         arr, len(mats), tau, kappa, seed, step, _stream(stream)))
 
 
+def maskllm_backward_stats_batched(mats, tau, kappa, seed, step, reg_coeff=0.0, stream=None):
+    """maskllm_backward_stats over a batch: the backward's fields (`W`,
+    `logits`, `grad_W_out`, `dlogits_out`) and the diagnostics' fields of
+    maskllm_mask_stats_batched."""
+    arr = matrix_array(mats)
+    _check("maskllm_backward_stats_batched", lib().maskllm_backward_stats_batched(
+        arr, len(mats), tau, kappa, seed, step, reg_coeff, _stream(stream)))
+
+
 def maskllm_set_wait_timeout(nanoseconds: int) -> None:
     _check("maskllm_set_wait_timeout", lib().maskllm_set_wait_timeout(int(nanoseconds)))
 
@@ -526,3 +539,29 @@ def maskllm_forward_stats(W, logits, tau, kappa, rng, prev_idx=None, W_out=None,
         _ptr(W), _ptr(logits), _ptr(prev_idx), rows, cols, tau, kappa, _rng(rng), _ptr(W_out),
         _ptr(row_sq), _ptr(idx), _ptr(l1), _ptr(mp), _stream(stream)))
     return W_out, row_sq, idx, l1, mp
+
+
+def maskllm_backward_stats(W, logits, grad_W_out, tau, kappa, rng, reg_coeff=0.0, prev_idx=None,
+                           dlogits_out=None, want_idx=True, want_l1=None, want_maxprob=True,
+                           stream=None):
+    """The backward and the step's diagnostics in one pass.  Returns
+    (dlogits, idx | None, l1 int32 | None, maxprob | None); l1 holds uint32
+    values in an int32 tensor."""
+    rows, cols = W.shape
+    g = cols // 4
+    _need(W, "W", torch.bfloat16, (rows, cols))
+    _need(logits, "logits", torch.float32, (rows, g, 6))
+    _need(grad_W_out, "grad_W_out", torch.bfloat16, (rows, cols))
+    if prev_idx is not None:
+        _need(prev_idx, "prev_idx", torch.uint8, (rows, g))
+    dlogits_out = _out(dlogits_out, "dlogits_out", torch.float32, (rows, g, 6), W)
+    dev = W.device
+    idx = torch.empty((rows, g), dtype=torch.uint8, device=dev) if want_idx else None
+    if want_l1 is None:
+        want_l1 = prev_idx is not None
+    l1 = torch.empty((rows,), dtype=torch.int32, device=dev) if want_l1 else None
+    mp = torch.empty((rows,), dtype=torch.float32, device=dev) if want_maxprob else None
+    _check("maskllm_backward_stats", lib().maskllm_backward_stats(
+        _ptr(W), _ptr(logits), _ptr(grad_W_out), _ptr(prev_idx), rows, cols, tau, kappa,
+        _rng(rng), reg_coeff, _ptr(dlogits_out), _ptr(idx), _ptr(l1), _ptr(mp), _stream(stream)))
+    return dlogits_out, idx, l1, mp

@@ -38,6 +38,7 @@ struct StreamMatrix {
   void* out2;         // forward: probs (nullable); compress: idx (nullable)
   void* out3 = nullptr;   // forward with diagnostics: L1 distance per row (u32)
   void* out4 = nullptr;   // forward with diagnostics: max-probability sum per row (fp32)
+  const void* P = nullptr;   // backward with diagnostics: previous draws (u8 per group)
   int64_t rows;
   int64_t cols;
   uint32_t tensor_id;
@@ -59,6 +60,11 @@ cudaError_t stream_mask_stats(const Device& d, const StreamMatrix* m, int n, flo
 // out3 = L1 per row, out4 = max-probability sum per row (all nullable).
 cudaError_t stream_forward_stats(const Device& d, const StreamMatrix* m, int n, float tau,
                                  float kappa, RngArgs rng, cudaStream_t s);
+// The backward (out0 = dlogits) with the diagnostics in the same pass: P =
+// previous draws, out1 = draws, out2 = L1 per row, out3 = max-probability
+// sum per row (all nullable; out2 needs P).
+cudaError_t stream_backward_stats(const Device& d, const StreamMatrix* m, int n, float tau,
+                                  float kappa, RngArgs rng, float reg_coeff, cudaStream_t s);
 // Logits from 2:4 codes, up to kMaxBatch matrices in one launch
 // (kernels_pack.cu): W = the codes (u32 [rows, cols/32]), out0 = logits.
 cudaError_t launch_prior_from_mask(const Device& d, const StreamMatrix* m, int n, float high,

@@ -44,7 +44,8 @@ bool overlaps(Span a, Span b) {
 }
 
 // Inputs and outputs of one call (all matrices of a batch together; at most
-// 3 inputs and 5 outputs per matrix: the forward with diagnostics).
+// 4 inputs (the backward with diagnostics) and 5 outputs (the forward with
+// diagnostics) per matrix).
 struct Spans {
   static constexpr int kCap = 8 * kMaxBatch;
   Span in[kCap];
@@ -208,9 +209,23 @@ maskllm_status check_forward_stats(const maskllm_matrix& m, Spans& sp) {
   return MASKLLM_OK;
 }
 
+maskllm_status check_backward_stats(const maskllm_matrix& m, Spans& sp) {
+  MK_TRY(check_backward(m, sp));
+  return check_diagnostics(m, sp);
+}
+
 maskllm_status finish(cudaError_t e) { return e == cudaSuccess ? MASKLLM_OK : cuda_fail(e); }
 
-enum class Op { kPrior, kForward, kBackward, kCompress, kPriorFromMask, kMaskStats, kForwardStats };
+enum class Op {
+  kPrior,
+  kForward,
+  kBackward,
+  kCompress,
+  kPriorFromMask,
+  kMaskStats,
+  kForwardStats,
+  kBackwardStats
+};
 
 struct Call {
   Op op;
@@ -261,6 +276,13 @@ StreamMatrix to_stream(const maskllm_matrix& m, Op op) {
       s.out3 = m.l1_row_out;
       s.out4 = m.maxprob_row_out;
       break;
+    case Op::kBackwardStats:
+      s.P = m.prev_idx;
+      s.out0 = m.dlogits_out;
+      s.out1 = m.idx_out;
+      s.out2 = m.l1_row_out;
+      s.out3 = m.maxprob_row_out;
+      break;
   }
   return s;
 }
@@ -275,14 +297,14 @@ maskllm_status check_matrix(Op op, const maskllm_matrix& m, Spans& sp) {
     case Op::kPriorFromMask: return check_prior_from_mask(m, sp);
     case Op::kMaskStats: return check_mask_stats(m, sp);
     case Op::kForwardStats: return check_forward_stats(m, sp);
+    case Op::kBackwardStats: return check_backward_stats(m, sp);
   }
   return MASKLLM_ERR_INVALID_ARG;
 }
 
 maskllm_status run(const Call& c, const maskllm_matrix* mats, int32_t n, cudaStream_t s) {
   if (mats == nullptr || n < 1) return MASKLLM_ERR_INVALID_ARG;
-  if (c.op == Op::kForward || c.op == Op::kBackward || c.op == Op::kMaskStats ||
-      c.op == Op::kForwardStats)
+  if (c.op != Op::kPrior && c.op != Op::kCompress && c.op != Op::kPriorFromMask)
     MK_TRY(check_temperature(c.tau, c.kappa));
   if (!isfinite(c.reg) || !isfinite(c.scale) || !isfinite(c.high) || !isfinite(c.low))
     return MASKLLM_ERR_INVALID_ARG;
@@ -331,6 +353,9 @@ maskllm_status run(const Call& c, const maskllm_matrix* mats, int32_t n, cudaStr
       case Op::kPriorFromMask: e = launch_prior_from_mask(d, sm, nb, c.high, c.low, s); break;
       case Op::kMaskStats: e = stream_mask_stats(d, sm, nb, c.tau, c.kappa, rng, s); break;
       case Op::kForwardStats: e = stream_forward_stats(d, sm, nb, c.tau, c.kappa, rng, s); break;
+      case Op::kBackwardStats:
+        e = stream_backward_stats(d, sm, nb, c.tau, c.kappa, rng, c.reg, s);
+        break;
     }
     if (e != cudaSuccess) return cuda_fail(e);
   }
@@ -537,6 +562,39 @@ maskllm_status maskllm_forward_stats_batched(const maskllm_matrix* mats, int32_t
   c.seed = seed;
   c.step = step;
   return maskllm::run(c, mats, n, stream);
+}
+
+maskllm_status maskllm_backward_stats_batched(const maskllm_matrix* mats, int32_t n, float tau,
+                                              float kappa, uint64_t seed, uint32_t step,
+                                              float reg_coeff, maskllm_stream_t stream) {
+  Call c{Op::kBackwardStats};
+  c.tau = tau;
+  c.kappa = kappa;
+  c.seed = seed;
+  c.step = step;
+  c.reg = reg_coeff;
+  return maskllm::run(c, mats, n, stream);
+}
+
+maskllm_status maskllm_backward_stats(const uint16_t* W, const float* logits,
+                                      const uint16_t* grad_W_out, const uint8_t* prev_idx,
+                                      int64_t rows, int64_t cols, float tau, float kappa,
+                                      maskllm_rng rng, float reg_coeff, float* dlogits_out,
+                                      uint8_t* idx_out, uint32_t* l1_row_out,
+                                      float* maxprob_row_out, maskllm_stream_t stream) {
+  maskllm_matrix m{};
+  m.W = W;
+  m.logits = logits;
+  m.grad_W_out = grad_W_out;
+  m.prev_idx = prev_idx;
+  m.rows = rows;
+  m.cols = cols;
+  m.tensor_id = rng.tensor_id;
+  m.dlogits_out = dlogits_out;
+  m.idx_out = idx_out;
+  m.l1_row_out = l1_row_out;
+  m.maxprob_row_out = maxprob_row_out;
+  return maskllm_backward_stats_batched(&m, 1, tau, kappa, rng.seed, rng.step, reg_coeff, stream);
 }
 
 maskllm_status maskllm_mask_stats(const float* logits, const uint8_t* prev_idx, int64_t rows,

@@ -210,6 +210,30 @@ def test_full_batch_of_fused_diagnostics_validates_every_span(L):
     assert L.maskllm_forward_stats_batched(arr, n, 1.0, 1.0, 0, 0, None) == ALIAS
 
 
+def test_backward_stats_validation(L):
+    from semi_structured_sparsity_gb300 import binding
+    r = _rng()
+    bs = L.maskllm_backward_stats
+    # W, logits, grad_W_out, prev_idx, rows, cols, tau, kappa, rng, reg, dlogits, idx, l1, maxprob
+    assert bs(A, B, None, None, 4, 64, 1.0, 1.0, r, 0.0, Cc, None, None, None, None) == INVALID
+    assert bs(A, B, D, None, 4, 64, 1.0, 1.0, r, 0.0, None, None, None, None, None) == INVALID
+    assert bs(A, B, D, None, 4, 64, 1.0, 1.0, r, 0.0, Cc, None, E, None, None) == INVALID  # L1, no prev
+    assert bs(A, B, D, None, 4, 64, 0.0, 1.0, r, 0.0, Cc, None, None, None, None) == INVALID
+    assert bs(A, B, D, None, 4, 64, 1.0, 1.0, r, float("nan"), Cc, None, None, None, None) == INVALID
+    assert bs(A, B, D, None, 1, (1 << 24) + 32, 1.0, 1.0, r, 0.0, Cc, None, None, None, E) == SHAPE
+    assert bs(A, B, D, E + 8, 4, 64, 1.0, 1.0, r, 0.0, Cc, None, None, None, None) == ALIGN
+    assert bs(A, B, D, E, 4, 64, 1.0, 1.0, r, 0.0, Cc, A + 32, None, None, None) == ALIAS
+    arr = (binding.maskllm_matrix * 2)()
+    arr[0] = _mat(W=A, logits=B, grad_W_out=D, dlogits_out=Cc)
+    arr[1] = _mat(W=A + 0x1000, logits=B + 0x1000, grad_W_out=D + 0x1000, dlogits_out=Cc + 0x1000,
+                  l1_row_out=E)
+    bb = L.maskllm_backward_stats_batched
+    assert bb(arr, 2, 1.0, 1.0, 0, 0, 0.0, None) == INVALID            # L1 without prev
+    arr[1].prev_idx = E + 0x100
+    arr[1].maxprob_row_out = Cc + 16                                    # over matrix 0's dlogits
+    assert bb(arr, 2, 1.0, 1.0, 0, 0, 0.0, None) == ALIAS
+
+
 def test_next_entry_points_validation(L):
     r = _rng()
     assert L.maskllm_prior_from_mask(A, 4, 64, float("inf"), 0.0, B, None) == INVALID

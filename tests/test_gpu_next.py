@@ -244,6 +244,69 @@ def test_diagnostics_batched_optional_outputs_per_matrix():
             assert torch.equal(f["row_sq_out"].view(torch.int32), rsq.view(torch.int32))
 
 
+@pytest.mark.parametrize("rows,cols", SHAPES)
+@pytest.mark.parametrize("tau,kappa,reg", [(1.0, 3.0, 0.0), (0.2, 500.0, 0.25)])
+def test_backward_stats_is_backward_plus_stats(rows, cols, tau, kappa, reg):
+    """The backward with the diagnostics: dlogits bit-identical to
+    maskllm_backward (and within its tolerance of the oracle), draws / L1 /
+    max probability bit-identical to maskllm_mask_stats and as the oracle."""
+    W, L, G = wl.random_case(rows, cols, seed=5 * rows + cols, device="cuda")
+    rng_prev, rng = (7, 30, 2), (7, 31, 2)
+    prev, _, _ = mk.maskllm_mask_stats(L, tau, kappa, rng_prev)
+    dl, idx, l1, mp = mk.maskllm_backward_stats(W, L, G, tau, kappa, rng, reg_coeff=reg,
+                                                prev_idx=prev)
+    dref = mk.maskllm_backward(W, L, G, tau, kappa, rng, reg_coeff=reg)
+    sidx, sl1, smp = mk.maskllm_mask_stats(L, tau, kappa, rng, prev_idx=prev)
+    torch.cuda.synchronize()
+    assert torch.equal(dl.view(torch.int32), dref.view(torch.int32))
+    assert torch.equal(idx, sidx) and torch.equal(l1, sl1)
+    assert torch.equal(mp.view(torch.int32), smp.view(torch.int32))
+    from tests._helpers import bits16
+    Lh = L.cpu().numpy()
+    want = orc.backward(bits16(W), Lh, bits16(G), tau, kappa, *rng, reg_coeff=reg)
+    assert_close(dl.cpu().numpy(), want, what="dlogits")
+    wprev, _, _ = orc.mask_stats(Lh, rows, cols, tau, kappa, *rng_prev)
+    widx, wl1, wmp = orc.mask_stats(Lh, rows, cols, tau, kappa, *rng, prev_idx=wprev)
+    assert_bits_equal(idx.cpu().numpy(), widx, "draws")
+    assert_bits_equal(l1.cpu().numpy().view(np.uint32), wl1.astype(np.uint32), "L1 per row")
+    assert_close(mp.cpu().numpy(), wmp, rtol=1e-5, atol=0, what="max-probability row sum")
+
+
+@pytest.mark.parametrize("n", [len(SHAPES), 20])
+def test_backward_stats_batched_match_single_calls(n):
+    """One batched launch (two for 20 matrices) over every test shape, each
+    matrix with its own tensor id; matrix 0 without previous draws (no L1),
+    matrix 1 without draws out: every output bit-identical to the single
+    call's."""
+    tau, kappa, seed, step, reg = 0.5, 40.0, 3, 12, 0.1
+    shapes = [SHAPES[i % len(SHAPES)] for i in range(n)]
+    mats = []
+    for i, (rows, cols) in enumerate(shapes):
+        W, L, G = wl.random_case(rows, cols, seed=600 + i, device="cuda")
+        g = cols // 4
+        prev = None if i == 0 else mk.maskllm_mask_stats(L, tau, kappa, (seed, step - 1, i))[0]
+        mats.append({"W": W, "logits": L, "grad_W_out": G, "tensor_id": i, "prev_idx": prev,
+                     "dlogits_out": torch.empty_like(L),
+                     "idx_out": None if i == 1 else torch.empty((rows, g), dtype=torch.uint8,
+                                                                device="cuda"),
+                     "l1_row_out": None if prev is None else torch.empty((rows,), dtype=torch.int32,
+                                                                         device="cuda"),
+                     "maxprob_row_out": torch.empty((rows,), device="cuda")})
+    mk.maskllm_backward_stats_batched(mats, tau, kappa, seed, step, reg)
+    torch.cuda.synchronize()
+    for i, m in enumerate(mats):
+        dl, idx, l1, mp = mk.maskllm_backward_stats(m["W"], m["logits"], m["grad_W_out"], tau,
+                                                    kappa, (seed, step, i), reg_coeff=reg,
+                                                    prev_idx=m["prev_idx"])
+        torch.cuda.synchronize()
+        assert torch.equal(m["dlogits_out"].view(torch.int32), dl.view(torch.int32))
+        if m["idx_out"] is not None:
+            assert torch.equal(m["idx_out"], idx)
+        if m["l1_row_out"] is not None:
+            assert torch.equal(m["l1_row_out"], l1)
+        assert torch.equal(m["maxprob_row_out"].view(torch.int32), mp.view(torch.int32))
+
+
 def test_forward_stats_optional_outputs():
     W, L, _ = wl.random_case(40, 256, seed=5, device="cuda")
     Wo, rsq, idx, l1, mp = mk.maskllm_forward_stats(W, L, 1.0, 3.0, (1, 2, 3), want_row_sq=False,
