@@ -125,10 +125,24 @@ def test_wait_timeout_sets_error_and_context_survives():
         mk.maskllm_backward(W, L, G, 1.0, 10.0, (0, 0, 0))
         assert mk.maskllm_device_status() == 6      # MASKLLM_ERR_TIMEOUT
         assert mk.maskllm_device_status() == 0      # read clears it
+        # every other pipelined kernel takes the same way out
+        prev = torch.zeros((8, 256), dtype=torch.uint8, device="cuda")
+        for run in (lambda: mk.maskllm_prior_init(W, 1.0),
+                    lambda: mk.maskllm_hard_compress(W, L),
+                    lambda: mk.maskllm_mask_stats(L, 1.0, 10.0, (0, 0, 0), prev_idx=prev),
+                    lambda: mk.maskllm_forward_stats(W, L, 1.0, 10.0, (0, 0, 0), prev_idx=prev),
+                    lambda: mk.maskllm_backward_stats(W, L, G, 1.0, 10.0, (0, 0, 0),
+                                                      prev_idx=prev)):
+            run()
+            assert mk.maskllm_device_status() == 6
+            assert mk.maskllm_device_status() == 0
     finally:
         mk.maskllm_test_withhold_loads(False)
         mk.maskllm_set_wait_timeout(2_000_000_000)
     Wo, sq, _ = mk.maskllm_forward(W, L, 1.0, 10.0, (0, 0, 0))
+    dl, idx, _, _ = mk.maskllm_backward_stats(W, L, G, 1.0, 10.0, (0, 0, 0))
     torch.cuda.synchronize()
     assert mk.maskllm_device_status() == 0
     assert_bf16_ulps(bits16(Wo), orc.forward(bits16(W), L.cpu().numpy(), 1.0, 10.0, 0)[0])
+    assert torch.equal(dl.view(torch.int32),
+                       mk.maskllm_backward(W, L, G, 1.0, 10.0, (0, 0, 0)).view(torch.int32))
