@@ -146,3 +146,82 @@ def test_wait_timeout_sets_error_and_context_survives():
     assert_bf16_ulps(bits16(Wo), orc.forward(bits16(W), L.cpu().numpy(), 1.0, 10.0, 0)[0])
     assert torch.equal(dl.view(torch.int32),
                        mk.maskllm_backward(W, L, G, 1.0, 10.0, (0, 0, 0)).view(torch.int32))
+
+
+def _random_shapes(rng, n):
+    """Row lengths that exercise every chunking case: short rows packed
+    several to a chunk, rows of exactly one chunk, long rows with a ragged
+    last chunk (also not a multiple of 64 groups), single rows."""
+    cols = [32, 64, 96, 1056, 2048, 4096, 4128, 5504, 6144, 11008]
+    return [(int(rng.integers(1, 70)), int(rng.choice(cols))) for _ in range(n)]
+
+
+@pytest.mark.parametrize("trial", range(6))
+def test_random_batches_equal_single_calls(trial):
+    """Seeded random batches (1 to 20 matrices, so up to two launches) of
+    random shapes: every batched stream operation -- prior, forward,
+    backward, hard-compress, the diagnostics alone and fused into the
+    forward and the backward -- writes exactly what its single-matrix call
+    writes, matrix by matrix."""
+    rng = np.random.default_rng(1000 + trial)
+    n = int(rng.integers(1, 21))
+    shapes = _random_shapes(rng, n)
+    tau, kappa, seed, step = float(rng.choice([0.3, 1.0, 2.0])), float(rng.choice([3.0, 40.0])), 9, 5
+    mats = _mats(shapes, seed=50 * trial)
+    for i, (m, (r, c)) in enumerate(zip(mats, shapes)):
+        g = c // 4
+        m["prev_idx"] = mk.maskllm_mask_stats(m["logits"], tau, kappa, (seed, step - 1, 100 + i))[0]
+        m["l1_row_out"] = torch.empty((r,), dtype=torch.int32, device="cuda")
+        m["maxprob_row_out"] = torch.empty((r,), device="cuda")
+        m["draws_out"] = torch.empty((r, g), dtype=torch.uint8, device="cuda")
+
+    def equal(a, b):
+        return torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
+
+    # prior, forward, backward, hard-compress
+    mk.maskllm_prior_init_batched(mats, 2.5)
+    mk.maskllm_forward_batched(mats, tau, kappa, seed, step)
+    mk.maskllm_backward_batched(mats, tau, kappa, seed, step, 0.0)
+    mk.maskllm_hard_compress_batched(mats)
+    torch.cuda.synchronize()
+    for i, (m, (r, c)) in enumerate(zip(mats, shapes)):
+        rng_i = (seed, step, 100 + i)
+        assert equal(m["logits_out"], mk.maskllm_prior_init(m["W"], 2.5))
+        Wo, sq, pr = mk.maskllm_forward(m["W"], m["logits"], tau, kappa, rng_i,
+                                        probs_out=torch.empty_like(m["logits"]))
+        assert equal(m["W_out"], Wo) and equal(m["row_sq_out"], sq) and equal(m["probs_out"], pr)
+        assert equal(m["dlogits_out"], mk.maskllm_backward(m["W"], m["logits"], m["grad_W_out"],
+                                                            tau, kappa, rng_i))
+        v, meta, idx = mk.maskllm_hard_compress(m["W"], m["logits"], want_idx=True)
+        assert equal(m["values_out"], v) and equal(m["meta_out"], meta) and equal(m["idx_out"], idx)
+
+    # the diagnostics: alone, with the forward, with the backward
+    diag = [dict(m, idx_out=m["draws_out"]) for m in mats]
+    mk.maskllm_mask_stats_batched([dict(d, W=None) for d in diag], tau, kappa, seed, step)
+    torch.cuda.synchronize()
+    for i, d in enumerate(diag):
+        idx, l1, mp = mk.maskllm_mask_stats(d["logits"], tau, kappa, (seed, step, 100 + i),
+                                            prev_idx=d["prev_idx"])
+        torch.cuda.synchronize()
+        assert equal(d["draws_out"], idx) and equal(d["l1_row_out"], l1)
+        assert equal(d["maxprob_row_out"], mp)
+    mk.maskllm_forward_stats_batched(diag, tau, kappa, seed, step)
+    torch.cuda.synchronize()
+    for i, d in enumerate(diag):
+        Wo, sq, idx, l1, mp = mk.maskllm_forward_stats(d["W"], d["logits"], tau, kappa,
+                                                       (seed, step, 100 + i),
+                                                       prev_idx=d["prev_idx"])
+        torch.cuda.synchronize()
+        assert equal(d["W_out"], Wo) and equal(d["row_sq_out"], sq)
+        assert equal(d["draws_out"], idx) and equal(d["l1_row_out"], l1)
+        assert equal(d["maxprob_row_out"], mp)
+    mk.maskllm_backward_stats_batched(diag, tau, kappa, seed, step, 0.0)
+    torch.cuda.synchronize()
+    for i, d in enumerate(diag):
+        dl, idx, l1, mp = mk.maskllm_backward_stats(d["W"], d["logits"], d["grad_W_out"], tau,
+                                                    kappa, (seed, step, 100 + i),
+                                                    prev_idx=d["prev_idx"])
+        torch.cuda.synchronize()
+        assert equal(d["dlogits_out"], dl)
+        assert equal(d["draws_out"], idx) and equal(d["l1_row_out"], l1)
+        assert equal(d["maxprob_row_out"], mp)
