@@ -315,3 +315,37 @@ def test_forward_stats_optional_outputs():
     torch.cuda.synchronize()
     assert rsq is None and idx is None and l1 is None and mp is None
     assert torch.equal(Wo.view(torch.int16), Wf.view(torch.int16))
+
+
+def test_diagnostics_on_the_longest_rows():
+    """Rows of 2^24 weights, the longest the diagnostics accept (4096
+    chunks a row, each row finished by one CTA; an L1 row sum is exact in
+    fp32 up to 2^24): the diagnostics pass and both fused passes against the
+    oracle, and the fused passes' forward and backward outputs against the
+    plain calls."""
+    from tests._helpers import ROWSQ_RTOL, assert_bf16_ulps, bits16
+    rows, cols = 2, 1 << 24
+    tau, kappa = 0.5, 20.0
+    W, L, G = wl.random_case(rows, cols, seed=4242, device="cuda")
+    rng_prev, rng = (3, 1, 9), (3, 2, 9)
+    prev, _, _ = mk.maskllm_mask_stats(L, tau, kappa, rng_prev)
+    idx, l1, mp = mk.maskllm_mask_stats(L, tau, kappa, rng, prev_idx=prev)
+    Wo, rsq, fidx, fl1, fmp = mk.maskllm_forward_stats(W, L, tau, kappa, rng, prev_idx=prev)
+    dl, bidx, bl1, bmp = mk.maskllm_backward_stats(W, L, G, tau, kappa, rng, prev_idx=prev)
+    dref = mk.maskllm_backward(W, L, G, tau, kappa, rng)
+    torch.cuda.synchronize()
+    for a, b in ((idx, fidx), (idx, bidx), (l1, fl1), (l1, bl1)):
+        assert torch.equal(a, b)
+    for a in (fmp, bmp):
+        assert torch.equal(a.view(torch.int32), mp.view(torch.int32))
+    assert torch.equal(dl.view(torch.int32), dref.view(torch.int32))
+    Lh = L.cpu().numpy()
+    wprev, _, _ = orc.mask_stats(Lh, rows, cols, tau, kappa, *rng_prev)
+    widx, wl1, wmp = orc.mask_stats(Lh, rows, cols, tau, kappa, *rng, prev_idx=wprev)
+    assert_bits_equal(prev.cpu().numpy(), wprev, "previous draws")
+    assert_bits_equal(idx.cpu().numpy(), widx, "draws")
+    assert_bits_equal(l1.cpu().numpy().view(np.uint32), wl1.astype(np.uint32), "L1 per row")
+    assert_close(mp.cpu().numpy(), wmp, rtol=1e-5, atol=0, what="max-probability row sum")
+    wW, wsq, _, _ = orc.forward(bits16(W), Lh, tau, kappa, *rng)
+    assert_bf16_ulps(bits16(Wo), wW)
+    assert_close(rsq.cpu().numpy(), wsq, rtol=ROWSQ_RTOL, atol=0, what="row_sq")
