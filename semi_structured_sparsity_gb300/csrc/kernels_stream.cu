@@ -623,6 +623,7 @@ struct StatsOp : OpBase<GPT, 4> {
   static constexpr uint32_t kPartStride = 8;
   static constexpr uint32_t kPrevOffset = kPartOffset + (kChunkGroups / GPT) * kPartStride;
   static constexpr uint32_t kStageBytes = kPrevOffset + kChunkGroups;
+  static_assert(kPrevOffset % 16 == 0, "the previous draws' copy starts on a 16-byte boundary");
 
   __device__ static bool want_row(const MatDesc& d, int q) {
     return q == 0 ? (d.out1 != nullptr && d.G != nullptr) : d.out2 != nullptr;
@@ -872,6 +873,20 @@ struct Layout {
   static constexpr uint32_t kChunkOff = kBarOff + 2 * Op::kStages * 8;
   static constexpr uint32_t kFlagOff = kChunkOff + Op::kStages * sizeof(Chunk);
   static constexpr uint32_t kBytes = kFlagOff + 16;
+
+  // Every shared-memory region a consumer writes lies inside its stage: the
+  // row partials of every consumer thread (short rows use one slot per
+  // thread), the staged output in every output buffer, and (as each op
+  // states beside its layout) the inputs.
+  static_assert(Op::kRowQuantities == 0 ||
+                    (4 * Op::kRowQuantities <= Op::kPartStride &&
+                     Op::kPartOffset + Op::kConsumers * Op::kPartStride <= Op::kStageBytes),
+                "row partials of every consumer lie inside the stage");
+  static_assert(!Op::kStaged || Op::kOutOffset + (Op::kOutBuffers - 1) * Op::kOutBufBytes +
+                                        kChunkGroups * Op::kOutBytesPerGroup <=
+                                    Op::kStageBytes,
+                "staged outputs lie inside the stage");
+  static_assert(Op::kStageBytes % 16 == 0, "stages start on 16-byte boundaries");
 };
 
 // The producer's wait for the consumers to release a stage.
