@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 BYTES_PER_WEIGHT = {"prior": 8.0, "forward": 10.0, "backward": 16.0, "hard_compress": 9.125}
 KERNELS = ("prior", "forward", "backward", "hard_compress")
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal (context beside the measured peak)
 METRIC = "weights/s (prior + forward + backward + hard-compress step)"
 
 
@@ -353,7 +354,8 @@ def run_gpu(args):
         gbs = BYTES_PER_WEIGHT[k] * blk.weights / per_kernel_s[k] / 1e9
         kernels[k] = {"us_per_step": round(per_kernel_s[k] * 1e6, 2),
                       "weights_per_s": blk.weights / per_kernel_s[k],
-                      "GB_per_s": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
+                      "GB_per_s": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
+                      "frac_of_nominal_hbm": round(gbs / NOMINAL_HBM_GBS, 4)}
     dominant = max(KERNELS, key=lambda k: per_kernel_s[k])
     # the dominant kernel's algorithmic bytes over its CUDA-event time (one
     # batched launch per step covers the whole block)
